@@ -1,0 +1,304 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, independent of the oracle's own code path.
+
+* a hand-derived closed-form example (tests/golden/forward_closed_form.json)
+  and a hand-worked align example (tests/golden/align_hand.json);
+* a scalar brute force (pure-Python loops, math.exp) on tiny shapes;
+* the merged-weight identity x(W + AB) = xW + xAB (LoRA merged into the base
+  weights, as the hybrid-attention decoder page does before serving);
+* adapter -1 and B = 0 both reduce the layer to the plain MoE;
+* one expert, top-1, weight 1 reduces the layer to a dense two-projection MLP,
+  and the dense linear to x W^T + per-adapter LoRA;
+* linearity of the combine in the gate weights (one-hot weights isolate one
+  expert);
+* the align step against a counting sort and its invariants.
+
+The last test plants mistakes in the oracle (on the CPU) and checks that at
+least one pin catches each one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import moe_lora_ref as ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _silu(v):
+    return v / (1.0 + math.exp(-v))
+
+
+# ----------------------------------------------------------------- fixtures
+def _rand_layer(rng, T, H, I, E, k, L, r, none=True, scale=1.0):
+    x = rng.standard_normal((T, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]) if T else np.zeros((0, k), int)
+    w = rng.random((T, k)) + 0.1
+    w /= w.sum(1, keepdims=True) if T else 1
+    lo = -1 if none else 0
+    lora = rng.integers(lo, L, size=T) if L else np.full(T, -1)
+    Wgu = rng.standard_normal((E, 2 * I, H)) * scale
+    Wd = rng.standard_normal((E, H, I)) * scale
+    Agu = rng.standard_normal((L, E, r, H))
+    Bgu = rng.standard_normal((L, E, 2 * I, r))
+    Ad = rng.standard_normal((L, E, r, I))
+    Bd = rng.standard_normal((L, E, H, r))
+    return dict(x=x, topk_ids=ids, topk_weights=w, lora_ids=lora, W_gate_up=Wgu,
+                W_down=Wd, A_gu=Agu, B_gu=Bgu, A_d=Ad, B_d=Bd)
+
+
+def _brute(d):
+    """Scalar restatement: per token, per routed pair, explicit index sums."""
+    x, ids, w, lora = d["x"], d["topk_ids"], d["topk_weights"], d["lora_ids"]
+    Wgu, Wd = d["W_gate_up"], d["W_down"]
+    T, H = x.shape
+    k = ids.shape[1]
+    I = Wd.shape[2]
+    r = d["A_gu"].shape[2] if d["A_gu"].size else 0
+    out = [[0.0] * H for _ in range(T)]
+    for t in range(T):
+        a = int(lora[t])
+        for j in range(k):
+            e = int(ids[t, j])
+            g = [sum(x[t, h] * Wgu[e, c, h] for h in range(H)) for c in range(2 * I)]
+            if a >= 0:
+                z = [sum(x[t, h] * d["A_gu"][a, e, q, h] for h in range(H)) for q in range(r)]
+                for c in range(2 * I):
+                    g[c] += sum(z[q] * d["B_gu"][a, e, c, q] for q in range(r))
+            act = [_silu(g[i]) * g[I + i] for i in range(I)]
+            dd = [sum(act[i] * Wd[e, h, i] for i in range(I)) for h in range(H)]
+            if a >= 0:
+                z2 = [sum(act[i] * d["A_d"][a, e, q, i] for i in range(I)) for q in range(r)]
+                for h in range(H):
+                    dd[h] += sum(z2[q] * d["B_d"][a, e, h, q] for q in range(r))
+            for h in range(H):
+                out[t][h] += w[t, j] * dd[h]
+    return np.array(out)
+
+
+def _fwd(d, **kw):
+    return ref.moe_lora_forward_ref(d["x"], d["topk_ids"], d["topk_weights"], d["lora_ids"],
+                                    d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"],
+                                    d["A_d"], d["B_d"], **kw)
+
+
+def _rel(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# -------------------------------------------------------------------- pins
+def pin_closed_form():
+    g = json.load(open(os.path.join(GOLDEN, "forward_closed_form.json")))
+    d = {k: np.array(v, dtype=np.float64) for k, v in g.items()
+         if k not in ("source", "layout", "derivation")}
+    d["topk_ids"] = d["topk_ids"].astype(int)
+    d["lora_ids"] = d["lora_ids"].astype(int)
+    out = _fwd(d)
+    act0 = _silu(2.5) * 2
+    act1 = _silu(4.0) * 1
+    out0 = [0.75 * 2 * act0, 0.75 * 2 * act0 + 0.25 * 0.5 * act1]
+    b1 = _silu(-1.0) * -0.5
+    b0 = _silu(0.5) * -1.0
+    out1 = [0.5 * -b1 + 0.5 * b0, 0.5 * 0.5 * b1 + 0.5 * 2 * b0]
+    return np.abs(out - np.array([out0, out1])).max() < 1e-14
+
+
+def pin_brute_force(seed=0):
+    rng = np.random.default_rng(seed)
+    ok = True
+    for (T, H, I, E, k, L, r) in [(5, 6, 3, 4, 2, 3, 2), (3, 4, 5, 3, 3, 2, 1), (4, 3, 2, 2, 1, 1, 3)]:
+        d = _rand_layer(rng, T, H, I, E, k, L, r)
+        ok &= _rel(_fwd(d), _brute(d)) < 1e-12
+    return bool(ok)
+
+
+def pin_merged_identity(seed=1):
+    """x(W + AB) = xW + xAB for both projections: merge each adapter into each
+    expert's weights (stored layout: W' = W + B @ A) and run without LoRA."""
+    rng = np.random.default_rng(seed)
+    d = _rand_layer(rng, T=24, H=12, I=10, E=4, k=2, L=3, r=4)
+    out = _fwd(d)
+    ok = True
+    for a in range(-1, 3):
+        m = np.nonzero(d["lora_ids"] == a)[0]
+        if not len(m):
+            continue
+        dm = dict(d)
+        if a >= 0:
+            dm["W_gate_up"] = d["W_gate_up"] + np.einsum("ecq,eqh->ech", d["B_gu"][a], d["A_gu"][a])
+            dm["W_down"] = d["W_down"] + np.einsum("ehq,eqi->ehi", d["B_d"][a], d["A_d"][a])
+        dm["lora_ids"] = np.full_like(d["lora_ids"], -1)
+        ok &= _rel(_fwd(dm, tokens=m), out[m]) < 1e-12
+    return bool(ok)
+
+
+def pin_base_moe(seed=2):
+    """Adapter -1 everywhere, or B = 0, gives the plain MoE (computed here by
+    torch's float64 matmul per pair, a library routine)."""
+    import torch
+    rng = np.random.default_rng(seed)
+    d = _rand_layer(rng, T=20, H=16, I=8, E=5, k=3, L=2, r=4)
+    dn = dict(d, lora_ids=np.full(20, -1))
+    dz = dict(d, B_gu=np.zeros_like(d["B_gu"]), B_d=np.zeros_like(d["B_d"]))
+    x = torch.tensor(d["x"])
+    exp = torch.zeros(20, 16, dtype=torch.float64)
+    for t in range(20):
+        for j in range(3):
+            e = int(d["topk_ids"][t, j])
+            g = torch.tensor(d["W_gate_up"][e]) @ x[t]
+            act = torch.nn.functional.silu(g[:8]) * g[8:]
+            exp[t] += float(d["topk_weights"][t, j]) * (torch.tensor(d["W_down"][e]) @ act)
+    exp = exp.numpy()
+    return bool(_rel(_fwd(dn), exp) < 1e-12 and _rel(_fwd(dz), exp) < 1e-12)
+
+
+def pin_dense_reduction(seed=3):
+    """E = 1, top-1, weight 1: the layer is a dense two-projection MLP with
+    per-token LoRA; the dense linear is x W^T + (x A^T) B^T per adapter."""
+    rng = np.random.default_rng(seed)
+    d = _rand_layer(rng, T=9, H=6, I=5, E=1, k=1, L=3, r=2)
+    d["topk_weights"] = np.ones((9, 1))
+    y_gu = ref.moe_lora_linear_ref(d["x"], d["lora_ids"], d["W_gate_up"][0],
+                                   d["A_gu"][:, 0], d["B_gu"][:, 0])
+    act = np.array([[_silu(v) for v in row[:5]] for row in y_gu]) * y_gu[:, 5:]
+    y_d = ref.moe_lora_linear_ref(act, d["lora_ids"], d["W_down"][0], d["A_d"][:, 0], d["B_d"][:, 0])
+    ok = _rel(_fwd(d), y_d) < 1e-12
+    # dense linear against explicit per-token sums
+    x, W, A, B, lo = d["x"], d["W_gate_up"][0], d["A_gu"][:, 0], d["B_gu"][:, 0], d["lora_ids"]
+    exp = np.zeros((9, 10))
+    for t in range(9):
+        for n in range(10):
+            s = sum(x[t, h] * W[n, h] for h in range(6))
+            if lo[t] >= 0:
+                s += sum(sum(x[t, h] * A[lo[t], q, h] for h in range(6)) * B[lo[t], n, q]
+                         for q in range(2))
+            exp[t, n] = s
+    ok &= _rel(y_gu, exp) < 1e-12
+    return bool(ok)
+
+
+def pin_linearity(seed=4):
+    rng = np.random.default_rng(seed)
+    d = _rand_layer(rng, T=10, H=8, I=6, E=4, k=2, L=2, r=2)
+    out = _fwd(d)
+    ok = _rel(_fwd(dict(d, topk_weights=3.0 * d["topk_weights"])), 3.0 * out) < 1e-13
+    # one-hot: only j=0 counts -> equals the top-1 layer on the first expert
+    oh = np.zeros_like(d["topk_weights"])
+    oh[:, 0] = 1.0
+    d1 = dict(d, topk_ids=d["topk_ids"][:, :1], topk_weights=np.ones((10, 1)))
+    ok &= _rel(_fwd(dict(d, topk_weights=oh)), _fwd(d1)) < 1e-13
+    return bool(ok)
+
+
+def _counting_sort_align(topk_ids, lora_ids, E, L, bm):
+    """Align restated as a stable counting sort: walk entries in flat order,
+    append each to its (expert, adapter) bucket, then lay the buckets out."""
+    T, k = topk_ids.shape
+    buckets = {(e, a): [] for e in range(E) for a in range(-1, L)}
+    for f in range(T * k):
+        buckets[(int(topk_ids[f // k, f % k]), int(lora_ids[f // k]))].append(f)
+    sorted_ids, blk, seg = [], [], []
+    for e in range(E):
+        run = []
+        for a in range(-1, L):
+            seg.append(len(sorted_ids) + len(run))
+            run += buckets[(e, a)]
+        padded = run + [T * k] * ((-len(run)) % bm)
+        sorted_ids += padded
+        blk += [e] * (len(padded) // bm)
+    seg.append(len(sorted_ids))
+    return sorted_ids, blk, seg
+
+
+def pin_align(seed=5):
+    g = json.load(open(os.path.join(GOLDEN, "align_hand.json")))
+    ok = True
+    for c in g["cases"]:
+        out = ref.align_ref(np.array(c["topk_ids"]), np.array(c["lora_ids"]), c["E"], c["L"], c["block_m"])
+        ok &= out["sorted_ids"].tolist() == c["sorted_ids"]
+        ok &= out["blk_expert"].tolist() == c["blk_expert"]
+        ok &= out["seg_off"].tolist() == c["seg_off"]
+        ok &= out["num_post_pad"] == c["num_post_pad"]
+    rng = np.random.default_rng(seed)
+    for (T, k, E, L, bm) in [(50, 2, 8, 4, 16), (33, 3, 5, 2, 4), (1, 1, 1, 1, 8), (64, 4, 16, 3, 1)]:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+        lo = rng.integers(-1, L, size=T)
+        out = ref.align_ref(ids, lo, E, L, bm)
+        s, b, sg = _counting_sort_align(ids, lo, E, L, bm)
+        ok &= out["sorted_ids"].tolist() == s and out["blk_expert"].tolist() == b
+        ok &= out["seg_off"].tolist() == sg
+        # invariants
+        si = out["sorted_ids"]
+        ok &= sorted(si[si < T * k].tolist()) == list(range(T * k))
+        ok &= out["num_post_pad"] % bm == 0
+        ok &= bool(np.all(np.diff(out["blk_expert"]) >= 0))
+    return bool(ok)
+
+
+PINS = [pin_closed_form, pin_brute_force, pin_merged_identity, pin_base_moe,
+        pin_dense_reduction, pin_linearity, pin_align]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    assert pin()
+
+
+def test_oracle_token_subset():
+    rng = np.random.default_rng(7)
+    d = _rand_layer(rng, T=12, H=8, I=6, E=4, k=2, L=2, r=2)
+    full = _fwd(d)
+    sub = [7, 2, 11]
+    assert _rel(_fwd(d, tokens=sub), full[sub]) < 1e-13
+
+
+def test_oracle_bf16_conversion_exact():
+    bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x8000, 0x7F7F], dtype=np.uint16)
+    exp = [1.0, -1.0, 3.140625, 0.0, -0.0, 3.3895313892515355e38]
+    assert ref.as_f64(bits).tolist() == exp
+
+
+def test_oracle_rejects_bad_ids():
+    rng = np.random.default_rng(8)
+    d = _rand_layer(rng, T=4, H=4, I=2, E=3, k=1, L=2, r=1)
+    with pytest.raises(ValueError):
+        _fwd(dict(d, topk_ids=np.full((4, 1), 3)))
+    with pytest.raises(ValueError):
+        _fwd(dict(d, lora_ids=np.array([0, 1, 2, -1])))
+    with pytest.raises(ValueError):
+        ref.align_ref(np.array([[0], [5]]), np.array([0, 0]), 3, 2, 4)
+
+
+# ------------------------------------------------------ planted mistakes
+def _mut_silu_sign(v):
+    return v / (1.0 + np.exp(v))
+
+
+def _mut_drop_lora(X, A, B):
+    return np.zeros((X.shape[0], B.shape[0]))
+
+
+def _mut_lora_transpose(X, A, B):
+    z = X @ A.T
+    return (z @ B.T) * 0.5 + (z @ B.T)[:, ::-1] * 0.5
+
+
+MUTATIONS = [("silu", _mut_silu_sign), ("_lora_delta", _mut_drop_lora),
+             ("_lora_delta", _mut_lora_transpose)]
+
+
+@pytest.mark.parametrize("name,mut", MUTATIONS, ids=["silu_sign", "drop_lora", "scramble_lora"])
+def test_pins_catch_planted_mistakes(monkeypatch, name, mut):
+    monkeypatch.setattr(ref, name, mut)
+    results = {p.__name__: p() for p in PINS if p is not pin_align}
+    assert not all(results.values()), results
+
+
+def test_pins_catch_align_mistake(monkeypatch):
+    orig = np.lexsort
+    # drop the flat-index tie break (unstable order within a segment)
+    monkeypatch.setattr(np, "lexsort", lambda keys: orig((-keys[0],) + tuple(keys[1:])))
+    assert not pin_align()
