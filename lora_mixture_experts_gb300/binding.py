@@ -1,0 +1,215 @@
+"""ctypes binding of libmoelora.so -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls (declared in
+``include/moelora.h``), takes torch tensors for the device buffers and
+passes their data pointers and the current CUDA stream.  All arithmetic
+happens in the library's kernels; if the library is missing, ``load()``
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+_LIB = None
+
+MOELORA_OK = 0
+STATUS = {
+    0: "MOELORA_OK", -1: "MOELORA_ERR_INVALID_ARG", -2: "MOELORA_ERR_UNSUPPORTED",
+    -3: "MOELORA_ERR_MISALIGNED", -4: "MOELORA_ERR_WORKSPACE", -5: "MOELORA_ERR_CUDA",
+    -6: "MOELORA_ERR_BAD_INDEX", -7: "MOELORA_ERR_TIMEOUT",
+}
+
+
+class MoeLoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class moelora_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "k", "E", "H", "I", "L", "r")]
+
+
+class moelora_linear_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "K", "N", "L", "r")]
+
+
+_P = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+_I32 = ctypes.c_int32
+_SIGS = {
+    "moelora_workspace_bytes": (_SZ, [ctypes.POINTER(moelora_dims)]),
+    "moelora_linear_workspace_bytes": (_SZ, [ctypes.POINTER(moelora_linear_dims)]),
+    "moelora_align_workspace_bytes": (_SZ, [ctypes.POINTER(moelora_dims)]),
+    "moelora_align_capacity": (_SZ, [ctypes.POINTER(moelora_dims), _I32]),
+    "moe_lora_align": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _I32, _P, _P, _P, _P,
+                                      _P, _SZ, _P]),
+    "moe_lora_forward": (ctypes.c_int, [ctypes.POINTER(moelora_dims)] + [_P] * 12 + [_SZ, _P]),
+    "moe_lora_linear": (ctypes.c_int, [ctypes.POINTER(moelora_linear_dims)] + [_P] * 7 + [_SZ, _P]),
+    "moelora_set_timing_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _I32]),
+    "moelora_last_launch_count": (_I32, []),
+    "moelora_last_launch_name": (ctypes.c_char_p, [_I32]),
+    "moelora_get_error": (ctypes.c_int, [_P, _P]),
+    "moelora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load the library (building it first if it is missing and nvcc exists)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise FileNotFoundError(f"{path} is not built; run lora_mixture_experts_gb300.build")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def exported_symbols() -> Sequence[str]:
+    return list(_SIGS)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors are required")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensors are required")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != MOELORA_OK:
+        raise MoeLoraError(st, where)
+
+
+def dims_of(x, topk_ids, W_gate_up, W_down, A_gu=None) -> moelora_dims:
+    T, H = x.shape
+    E, two_i, _ = W_gate_up.shape
+    L, r = (A_gu.shape[0], A_gu.shape[2]) if A_gu is not None else (0, 0)
+    return moelora_dims(T, topk_ids.shape[1], E, H, two_i // 2, L, r)
+
+
+def moelora_workspace_bytes(d: moelora_dims) -> int:
+    return load().moelora_workspace_bytes(ctypes.byref(d))
+
+
+def moelora_linear_workspace_bytes(d: moelora_linear_dims) -> int:
+    return load().moelora_linear_workspace_bytes(ctypes.byref(d))
+
+
+def moelora_align_workspace_bytes(d: moelora_dims) -> int:
+    return load().moelora_align_workspace_bytes(ctypes.byref(d))
+
+
+def moelora_align_capacity(d: moelora_dims, block_m: int) -> int:
+    return load().moelora_align_capacity(ctypes.byref(d), block_m)
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def moe_lora_align(topk_ids, lora_ids, E: int, L: int, block_m: int, ws=None, stream=None):
+    """Returns (sorted_ids, blk_expert, seg_off, num_post_pad) device tensors."""
+    lib = load()
+    T, k = topk_ids.shape
+    d = moelora_dims(T, k, E, 8, 8, L, 0)
+    cap = lib.moelora_align_capacity(ctypes.byref(d), block_m)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    blk = torch.empty(max(cap // max(block_m, 1), 1), dtype=torch.int32, device=dev)
+    seg = torch.empty(E * (L + 1) + 1, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(lib.moelora_align_workspace_bytes(ctypes.byref(d)), dev)
+    st = lib.moe_lora_align(ctypes.byref(d), _ptr(topk_ids), _ptr(lora_ids), block_m,
+                            _ptr(sorted_ids), _ptr(blk), _ptr(seg), _ptr(npp), _ptr(ws),
+                            ws.numel(), _stream(stream))
+    _check(st, "moe_lora_align")
+    return sorted_ids[:cap], blk[:cap // block_m], seg, npp
+
+
+def moe_lora_forward(x, topk_ids, topk_weights, lora_ids, W_gate_up, W_down,
+                     A_gu=None, B_gu=None, A_d=None, B_d=None, out=None, ws=None, stream=None):
+    """The fused MoE-LoRA expert layer; returns out[T,H] bf16."""
+    lib = load()
+    d = dims_of(x, topk_ids, W_gate_up, W_down, A_gu)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = alloc_workspace(lib.moelora_workspace_bytes(ctypes.byref(d)), x.device)
+    st = lib.moe_lora_forward(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                              _ptr(lora_ids), _ptr(W_gate_up), _ptr(W_down), _ptr(A_gu),
+                              _ptr(B_gu), _ptr(A_d), _ptr(B_d), _ptr(out), _ptr(ws), ws.numel(),
+                              _stream(stream))
+    _check(st, "moe_lora_forward")
+    return out
+
+
+def moe_lora_linear(x, lora_ids, W, A=None, B=None, out=None, ws=None, stream=None):
+    """Dense multi-LoRA linear; returns out[T,N] bf16."""
+    lib = load()
+    T, K = x.shape
+    N = W.shape[0]
+    L, r = (A.shape[0], A.shape[1]) if A is not None else (0, 0)
+    d = moelora_linear_dims(T, K, N, L, r)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = alloc_workspace(lib.moelora_linear_workspace_bytes(ctypes.byref(d)), x.device)
+    st = lib.moe_lora_linear(ctypes.byref(d), _ptr(x), _ptr(lora_ids), _ptr(W), _ptr(A), _ptr(B),
+                             _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "moe_lora_linear")
+    return out
+
+
+def moelora_get_error(ws, stream=None) -> int:
+    return load().moelora_get_error(_ptr(ws), _stream(stream))
+
+
+def moelora_set_timing_events(events) -> None:
+    """Install (list of torch.cuda.Event) or remove (None) the per-launch timing hook."""
+    lib = load()
+    if not events:
+        _check(lib.moelora_set_timing_events(None, 0), "moelora_set_timing_events")
+        return
+    for e in events:
+        e.record() if e.cuda_event == 0 else None   # make sure the event exists
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib.moelora_set_timing_events(arr, len(events)), "moelora_set_timing_events")
+
+
+def moelora_last_launches():
+    lib = load()
+    n = lib.moelora_last_launch_count()
+    return [lib.moelora_last_launch_name(i).decode() for i in range(n)]
+
+
+def moelora_status_string(status: int) -> str:
+    return load().moelora_status_string(status).decode()

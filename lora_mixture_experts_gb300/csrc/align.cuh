@@ -1,0 +1,64 @@
+// Host-visible declarations of the align, permute and combine kernels
+// (align_kernels.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace moelora {
+
+constexpr int kAlignChunk = 256;        // entries per align CTA
+constexpr int kMaxBins = 11264;         // E*(L+1) held in one CTA's shared memory (44 KB)
+constexpr int kMaxExperts = 1024;
+
+struct AlignArgs {
+  // inputs
+  const int32_t* topk_ids;      // [T*k]; NULL = every entry on expert 0 (E == 1, k == 1)
+  const int32_t* lora_ids;      // [T]
+  const float* topk_weights;    // [T*k]; NULL = weight 1
+  int T, k, E, L;
+  int lora_ignore;               // 1: every entry's adapter is -1 (layer without LoRA)
+  int n;                        // T*k
+  int nbins;                    // E*(L+1)
+  int nchunks;                  // ceil(n / kAlignChunk)
+  int block_m;
+  int Pmax;
+  // scratch
+  int* chunk_hist;              // [nchunks][nbins] -> per-chunk offsets
+  int* bin_of;                  // [n]
+  int* rank_of;                 // [n]
+  int* bin_start;               // [nbins]
+  WsHeader* hdr;
+  // align outputs
+  int* sorted_ids;              // [Pmax]
+  int* blk_expert;              // [Pmax / block_m]
+  int* seg_off;                 // [nbins + 1], may be NULL
+  int* num_post_pad;            // [1], may be NULL
+  // forward extras (NULL for the plain align)
+  int* row_tok;                 // [Pmax] token of each sorted row, -1 for padding
+  int* row_lora;                // [Pmax] adapter of each row, -2 for padding
+  float* row_w;                 // [Pmax] gate weight of each row, 0 for padding
+  int* pos_of;                  // [n] sorted row of each entry, -1 if dropped
+  // token tiles, LoRA slots and shrink items for the GEMM phases
+  int tn;                       // token tile width
+  int spi;                      // slots per shrink item (128 / r); 0 = no LoRA
+  TileInfo* tiles;
+  ShrinkItem* shrink;
+  int* slot_adapter;
+  int* tile_done;
+};
+
+// The three align kernels; hist and scatter are skipped (return success)
+// when there are no entries.
+cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream);
+cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream);
+cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream);
+
+// x_perm[p] = x[row_tok[p]] (zero rows for padding), p < Pmax.
+cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
+                           int Pmax, int H, int num_sms, cudaStream_t stream);
+
+// out[t] = sum_j y_pair[pos_of[t*k+j]] in fp32, j ascending, one bf16 rounding.
+cudaError_t launch_combine(const __nv_bfloat16* y_pair, const int* pos_of, __nv_bfloat16* out,
+                           int T, int k, int H, int num_sms, cudaStream_t stream);
+
+}  // namespace moelora

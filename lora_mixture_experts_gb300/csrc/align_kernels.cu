@@ -1,0 +1,318 @@
+// Align (group routed entries by expert and adapter), permute and combine.
+//
+// Align follows the grouping of the multi-LoRA MoE blog ("Implementing
+// multi-LoRA for MoE in vLLM": fused_moe runs one GEMM per expert over its
+// tokens and fused_moe_lora adds a grid dimension over the active adapters).
+// The order is the stable sort of the entries by (expert, adapter+1), done as
+// a three-kernel counting sort that needs no atomics for positions:
+//   hist    -- per 256-entry chunk: bin of every entry, its rank among the
+//              chunk's earlier entries of the same bin, the chunk histogram;
+//   scan    -- one CTA: per-bin chunk offsets, expert counts, per-expert
+//              padding to block_m, segment offsets, padding rows, and the
+//              token-tile / LoRA-slot / shrink-item tables of the GEMMs;
+//   scatter -- position = bin start + chunk offset + rank.
+// Every position is a pure function of the inputs, so the result is
+// bit-identical run to run.
+#include "align.cuh"
+
+namespace moelora {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kAlignChunk) align_hist_kernel(AlignArgs a) {
+  __shared__ int bins[kAlignChunk];
+  extern __shared__ int hist[];   // [nbins]
+  const int c = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int f = c * kAlignChunk + tid;
+  int bin = -1;
+  if (f < a.n) {
+    const int e = a.topk_ids ? a.topk_ids[f] : 0;
+    const int l = a.lora_ignore ? -1 : a.lora_ids[f / a.k];
+    if (e < 0 || e >= a.E || l < -1 || l >= a.L)
+      flag_error(&a.hdr->err, kStatusBadIndex);
+    else
+      bin = e * (a.L + 1) + l + 1;
+  }
+  bins[tid] = bin;
+  for (int b = tid; b < a.nbins; b += kAlignChunk) hist[b] = 0;
+  __syncthreads();
+  if (bin >= 0) atomicAdd(&hist[bin], 1);
+  int rank = 0;
+  for (int i = 0; i < tid; ++i) rank += (bins[i] == bin);
+  if (f < a.n) {
+    a.bin_of[f] = bin;
+    a.rank_of[f] = rank;
+  }
+  __syncthreads();
+  int* out = a.chunk_hist + static_cast<size_t>(c) * a.nbins;
+  for (int b = tid; b < a.nbins; b += kAlignChunk) out[b] = hist[b];
+}
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;   // inclusive
+  }
+  __syncthreads();
+  const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  if (total) *total = warp_sums[31];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  const int Lp = a.L + 1;
+
+  // per-bin chunk offsets (in place) and totals (into bin_start)
+  for (int b = tid; b < a.nbins; b += kScanThreads) {
+    int run = 0;
+    for (int c = 0; c < a.nchunks; ++c) {
+      int* h = a.chunk_hist + static_cast<size_t>(c) * a.nbins + b;
+      const int v = *h;
+      *h = run;
+      run += v;
+    }
+    a.bin_start[b] = run;
+  }
+  __syncthreads();
+
+  // one expert per thread
+  const int e = tid;
+  const bool has_e = e < a.E;
+  int cnt = 0;
+  if (has_e)
+    for (int l = 0; l < Lp; ++l) cnt += a.bin_start[e * Lp + l];
+  const int pad = has_e ? (cnt + a.block_m - 1) / a.block_m * a.block_m : 0;
+  int P;
+  const int start = block_exclusive_scan(pad, warp_sums, &P);
+  // every thread read its own expert's totals above; each overwrites only its own bins
+
+  if (has_e) {
+    int s = start;
+    for (int l = 0; l < Lp; ++l) {
+      const int b = e * Lp + l;
+      const int tot = a.bin_start[b];
+      a.bin_start[b] = s;
+      if (a.seg_off) a.seg_off[b] = s;
+      s += tot;
+    }
+    for (int blk = start / a.block_m; blk < (start + pad) / a.block_m; ++blk) a.blk_expert[blk] = e;
+    for (int p = start + cnt; p < start + pad; ++p) {
+      a.sorted_ids[p] = a.n;
+      if (a.row_tok) {
+        a.row_tok[p] = -1;
+        a.row_lora[p] = -2;
+        a.row_w[p] = 0.0f;
+      }
+    }
+  }
+  for (int p = P + tid; p < a.Pmax; p += kScanThreads) {
+    a.sorted_ids[p] = a.n;
+    if (a.row_tok) {
+      a.row_tok[p] = -1;
+      a.row_lora[p] = -2;
+      a.row_w[p] = 0.0f;
+    }
+  }
+  for (int blk = P / a.block_m + tid; blk < a.Pmax / a.block_m; blk += kScanThreads)
+    a.blk_expert[blk] = -1;
+  if (tid == 0) {
+    if (a.seg_off) a.seg_off[a.nbins] = P;
+    if (a.num_post_pad) *a.num_post_pad = P;
+    a.hdr->P = P;
+  }
+  if (!a.tiles) return;   // plain align: no GEMM tables
+
+  // token tiles of tn rows per expert; one LoRA slot per adapter (>= 0)
+  // present in a tile; shrink items of up to spi slots
+  __syncthreads();
+  int n_t = 0, n_s = 0, n_h = 0;
+  if (has_e && cnt > 0) {
+    n_t = (cnt + a.tn - 1) / a.tn;
+    if (a.spi > 0) {
+      for (int j = 0; j < n_t; ++j) {
+        const int s0 = start + j * a.tn;
+        const int s1 = min(start + cnt, s0 + a.tn);
+        int ns = 0;
+        for (int l = 1; l < Lp; ++l) {
+          const int lo = a.bin_start[e * Lp + l];
+          const int hi = (l + 1 < Lp) ? a.bin_start[e * Lp + l + 1] : start + cnt;
+          if (lo < hi && lo < s1 && hi > s0) ++ns;
+        }
+        n_s += ns;
+        n_h += (ns + a.spi - 1) / a.spi;
+      }
+    }
+  }
+  int tot_t, tot_s, tot_h;
+  const int tbase = block_exclusive_scan(n_t, warp_sums, &tot_t);
+  const int sbase = block_exclusive_scan(n_s, warp_sums, &tot_s);
+  const int hbase = block_exclusive_scan(n_h, warp_sums, &tot_h);
+  if (has_e && cnt > 0) {
+    int sl = sbase, sh = hbase;
+    for (int j = 0; j < n_t; ++j) {
+      const int s0 = start + j * a.tn;
+      const int s1 = min(start + cnt, s0 + a.tn);
+      TileInfo ti;
+      ti.expert = e;
+      ti.row0 = s0;
+      ti.nrows = s1 - s0;
+      ti.slot_base = sl;
+      ti.sh_base = sh;
+      ti.pad_ = 0;
+      int ns = 0;
+      if (a.spi > 0) {
+        for (int l = 1; l < Lp; ++l) {
+          const int lo = a.bin_start[e * Lp + l];
+          const int hi = (l + 1 < Lp) ? a.bin_start[e * Lp + l + 1] : start + cnt;
+          if (lo < hi && lo < s1 && hi > s0) a.slot_adapter[sl + ns++] = l - 1;
+        }
+      }
+      ti.nslots = ns;
+      const int nh = a.spi > 0 ? (ns + a.spi - 1) / a.spi : 0;
+      ti.nsh = nh;
+      for (int h = 0; h < nh; ++h) {
+        ShrinkItem si;
+        si.tile = tbase + j;
+        si.slot0 = sl + h * a.spi;
+        si.nslot = min(a.spi, ns - h * a.spi);
+        si.pad_ = 0;
+        a.shrink[sh + h] = si;
+      }
+      a.tiles[tbase + j] = ti;
+      a.tile_done[tbase + j] = 0;
+      sl += ns;
+      sh += nh;
+    }
+  }
+  if (tid == 0) {
+    a.hdr->n_tiles = tot_t;
+    a.hdr->n_slots = tot_s;
+    a.hdr->n_shrink = tot_h;
+  }
+}
+
+__global__ void __launch_bounds__(kAlignChunk) align_scatter_kernel(AlignArgs a) {
+  const int c = blockIdx.x;
+  const int f = c * kAlignChunk + threadIdx.x;
+  if (f >= a.n) return;
+  const int bin = a.bin_of[f];
+  if (bin < 0) {
+    if (a.pos_of) a.pos_of[f] = -1;
+    return;
+  }
+  const int pos = a.bin_start[bin] + a.chunk_hist[static_cast<size_t>(c) * a.nbins + bin] +
+                  a.rank_of[f];
+  a.sorted_ids[pos] = f;
+  if (a.row_tok) {
+    a.row_tok[pos] = f / a.k;
+    a.row_lora[pos] = bin % (a.L + 1) - 1;
+    a.row_w[pos] = a.topk_weights ? a.topk_weights[f] : 1.0f;
+    a.pos_of[f] = pos;
+  }
+}
+
+__global__ void permute_kernel(const uint4* __restrict__ x, const int* __restrict__ row_tok,
+                               uint4* __restrict__ x_perm, int Pmax, int hv) {
+  const size_t total = static_cast<size_t>(Pmax) * hv;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(i / hv);
+    const int c = static_cast<int>(i - static_cast<size_t>(p) * hv);
+    const int t = row_tok[p];
+    x_perm[i] = t >= 0 ? x[static_cast<size_t>(t) * hv + c] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void combine_kernel(const uint4* __restrict__ y_pair, const int* __restrict__ pos_of,
+                               uint4* __restrict__ out, int T, int k, int hv) {
+  const size_t total = static_cast<size_t>(T) * hv;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / hv);
+    const int c = static_cast<int>(i - static_cast<size_t>(t) * hv);
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int pos = pos_of[t * k + j];
+      if (pos < 0) continue;
+      const uint4 v = y_pair[static_cast<size_t>(pos) * hv + c];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f2 = __bfloat1622float2(h2[q]);
+        acc[2 * q] += f2.x;
+        acc[2 * q + 1] += f2.y;
+      }
+    }
+    uint4 o;
+    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o2[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    out[i] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream) {
+  if (a.nchunks == 0) return cudaSuccess;
+  align_hist_kernel<<<a.nchunks, kAlignChunk, a.nbins * sizeof(int), stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream) {
+  align_scan_kernel<<<1, kScanThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream) {
+  if (a.nchunks == 0) return cudaSuccess;
+  align_scatter_kernel<<<a.nchunks, kAlignChunk, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
+                           int Pmax, int H, int num_sms, cudaStream_t stream) {
+  const int hv = H / 8;
+  const size_t total = static_cast<size_t>(Pmax) * hv;
+  int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
+  if (grid < 1) grid = 1;
+  permute_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), row_tok,
+                                           reinterpret_cast<uint4*>(x_perm), Pmax, hv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const __nv_bfloat16* y_pair, const int* pos_of, __nv_bfloat16* out,
+                           int T, int k, int H, int num_sms, cudaStream_t stream) {
+  const int hv = H / 8;
+  const size_t total = static_cast<size_t>(T) * hv;
+  int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
+  if (grid < 1) grid = 1;
+  combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(y_pair), pos_of,
+                                           reinterpret_cast<uint4*>(out), T, k, hv);
+  return cudaGetLastError();
+}
+
+}  // namespace moelora

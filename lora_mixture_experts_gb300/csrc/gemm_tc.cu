@@ -1,0 +1,428 @@
+// Persistent tcgen05 grouped GEMM for the MoE-LoRA expert layer (sm_103a).
+//
+// One launch runs one projection phase of the layer (multi-LoRA MoE blog,
+// "Implementing multi-LoRA for MoE in vLLM": y = xW + xAB per projection,
+// the shrink z = xA and the expand zB, one GEMM per expert over its tokens):
+//
+//  * shrink items  -- z = X A[a,e]^T for the adapters present in a token tile,
+//    stacked r rows per adapter in one 128-row MMA tile.  The epilogue keeps,
+//    for every token, only the rows of its own adapter and writes zeros for
+//    the others, so the expand can treat each adapter as one extra K-chunk.
+//  * main items    -- a 128-row tile of the expert's weight rows against one
+//    token tile: acc = W_tile X^T (K loop over the hidden size) followed by
+//    one K-chunk of width r per adapter present: acc += B[a,e]_tile Z_a^T.
+//    The epilogue applies SiLU(gate)*up (gate_up), the gate weight (down) or
+//    nothing (dense linear) and stores bf16.
+//
+// Orientation: the weight rows are the MMA's M side (128 rows) and the
+// tokens its N side (16..256, rounded up to 16), so a decode-sized tile with
+// a few tokens streams weights at full width and a prefill tile uses N=256.
+// Operands arrive by TMA (128-byte swizzle, K-major) into a ring of shared
+// memory stages; one thread issues tcgen05.mma into a double-buffered TMEM
+// accumulator; four epilogue warps drain TMEM with tcgen05.ld.
+//
+// Shrink items precede main items in the item order and a main item's
+// producer waits (bounded) for its tile's shrink items before loading the
+// z chunks.  Every CTA of the persistent grid is resident at once (grid <=
+// SM count, one CTA per SM), so the wait always ends.
+#include "gemm_tc.cuh"
+
+namespace moelora {
+namespace {
+
+constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
+constexpr int kXchgStride = 17;          // floats per row of the gate/up exchange
+
+template <int TN>
+struct Cfg {
+  static constexpr int kStages = TN >= 256 ? 4 : 10;
+  static constexpr int kBTileBytes = TN * 128;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kNumBoxes = TN >= 256 ? 5 : (TN >= 128 ? 4 : (TN >= 64 ? 3 : (TN >= 32 ? 2 : 1)));
+  static constexpr int kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;
+  static constexpr int kXchgBytes = 64 * kXchgStride * 4;
+  static constexpr int kBarOff = kStages * kStageBytes + kXchgBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+};
+
+struct Item {
+  int shrink;   // 1 = shrink item
+  int tile;
+  int m;        // weight tile (main items)
+  int sh;       // shrink item index
+};
+
+__device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, const ShrinkItem* sh) {
+  Item it;
+  if (w < n_sh) {
+    it.shrink = 1;
+    it.sh = w;
+    it.tile = sh[w].tile;
+    it.m = 0;
+  } else {
+    w -= n_sh;
+    it.shrink = 0;
+    it.sh = -1;
+    it.tile = w % n_tiles;
+    it.m = w / n_tiles;
+  }
+  return it;
+}
+
+// Smallest box index i with (16 << i) >= n.
+__device__ __forceinline__ int box_index(int n) {
+  int i = 0;
+  while ((16 << i) < n) ++i;
+  return i;
+}
+
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+template <int TN>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using C = Cfg<TN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + C::kStages;
+  uint64_t* accf_bar = bars + 2 * C::kStages;       // [2]
+  uint64_t* acce_bar = bars + 2 * C::kStages + 2;   // [2]
+  uint64_t* drain_bar = bars + 2 * C::kStages + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&accf_bar[b]), 1);
+      mbar_init(smem_u32(&acce_bar[b]), 4);
+    }
+    mbar_init(smem_u32(drain_bar), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.w);
+    if (p.r > 0) {
+      tma_prefetch_desc(&maps.lb);
+      tma_prefetch_desc(&maps.la);
+    }
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int n_tiles = p.hdr->n_tiles;
+  const int n_sh = p.r > 0 ? p.hdr->n_shrink : 0;
+  const int n_items = n_sh + n_tiles * p.n_mtiles;
+  const int nk = (p.K + 63) / 64;
+  const bool gate_up = p.mode == kModeGateUp;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t cnt = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const Item it = decode_item(w, n_sh, n_tiles, p.shrink);
+        const TileInfo ti = p.tiles[it.tile];
+        const int nmma = (ti.nrows + 15) & ~15;
+        const int bi = box_index(nmma);
+        const int brows = 16 << bi;
+        const CUtensorMap* tb = &maps.b[bi];
+        if (it.shrink) {
+          const ShrinkItem si = p.shrink[it.sh];
+          const uint32_t bytes = si.nslot * p.r * 128 + brows * 128;
+          for (int kc = 0; kc < nk && ok; ++kc, ++cnt) {
+            const int s = cnt % C::kStages;
+            const uint32_t ph = (cnt / C::kStages) & 1;
+            if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
+            const uint32_t fb = smem_u32(&full_bar[s]);
+            const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
+            mbar_arrive_expect_tx(fb, bytes);
+            for (int j = 0; j < si.nslot; ++j)
+              tma_load_4d(a_s + j * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
+                          p.slot_adapter[si.slot0 + j]);
+            tma_load_2d(a_s + kATileBytes, tb, fb, kc * 64, ti.row0);
+          }
+        } else {
+          const uint32_t bytes = kATileBytes + brows * 128;
+          for (int kc = 0; kc < nk && ok; ++kc, ++cnt) {
+            const int s = cnt % C::kStages;
+            const uint32_t ph = (cnt / C::kStages) & 1;
+            if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
+            const uint32_t fb = smem_u32(&full_bar[s]);
+            const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
+            mbar_arrive_expect_tx(fb, bytes);
+            if (gate_up) {
+              tma_load_3d(a_s, &maps.w, fb, kc * 64, it.m * 64, ti.expert);
+              tma_load_3d(a_s + 64 * 128, &maps.w, fb, kc * 64, p.half_rows + it.m * 64, ti.expert);
+            } else {
+              tma_load_3d(a_s, &maps.w, fb, kc * 64, it.m * 128, ti.expert);
+            }
+            tma_load_2d(a_s + kATileBytes, tb, fb, kc * 64, ti.row0);
+          }
+          if (ok && p.r > 0 && ti.nslots > 0) {
+            // the tile's shrink results must be complete and visible to TMA
+            const int target = p.done_target * ti.nsh;
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(&p.tile_done[it.tile]) < target) {
+              if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+            fence_proxy_async_global();
+            const CUtensorMap* tz = &maps.z[bi];
+            const int lw = p.lora_w;
+            const uint32_t bytes_l = 128 * lw * 2 + brows * lw * 2;
+            for (int sl = 0; sl < ti.nslots && ok; ++sl) {
+              const int a = p.slot_adapter[ti.slot_base + sl];
+              for (int c = 0; c < p.lora_chunks && ok; ++c, ++cnt) {
+                const int s = cnt % C::kStages;
+                const uint32_t ph = (cnt / C::kStages) & 1;
+                if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
+                const uint32_t fb = smem_u32(&full_bar[s]);
+                const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
+                mbar_arrive_expect_tx(fb, bytes_l);
+                if (gate_up) {
+                  tma_load_4d(a_s, &maps.lb, fb, c * lw, it.m * 64, ti.expert, a);
+                  tma_load_4d(a_s + 64 * lw * 2, &maps.lb, fb, c * lw, p.half_rows + it.m * 64,
+                              ti.expert, a);
+                } else {
+                  tma_load_4d(a_s, &maps.lb, fb, c * lw, it.m * 128, ti.expert, a);
+                }
+                tma_load_2d(a_s + kATileBytes, tz, fb, c * lw, (ti.slot_base + sl) * TN);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        flag_error(p.err, kStatusTimeout);
+        // let the copies already issued land before the CTA exits
+        const uint32_t first = cnt > (uint32_t)C::kStages ? cnt - C::kStages : 0;
+        for (uint32_t c = first; c < cnt; ++c) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&full_bar[c % C::kStages]), (c / C::kStages) & 1))
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t cnt = 0;
+      uint32_t li = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++li) {
+        const Item it = decode_item(w, n_sh, n_tiles, p.shrink);
+        const TileInfo ti = p.tiles[it.tile];
+        const int nmma = (ti.nrows + 15) & ~15;
+        const uint32_t idesc = make_idesc_bf16(nmma);
+        const int buf = li & 1;
+        if (!(ok = mbar_wait(smem_u32(&acce_bar[buf]), ((li >> 1) & 1) ^ 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * TN;
+        const int n_lora = (!it.shrink && p.r > 0) ? ti.nslots * p.lora_chunks : 0;
+        const int nch = nk + n_lora;
+        for (int ch = 0; ch < nch; ++ch, ++cnt) {
+          const int s = cnt % C::kStages;
+          const uint32_t ph = (cnt / C::kStages) & 1;
+          if (!(ok = mbar_wait(smem_u32(&full_bar[s]), ph, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t b_s = a_s + kATileBytes;
+          const bool base = ch < nk;
+          const int width = base ? 64 : p.lora_w;
+          const uint32_t swz = base ? 2u : static_cast<uint32_t>(p.lora_swz);
+          const uint32_t sbo = base ? 1024u : static_cast<uint32_t>(8 * p.lora_w * 2);
+          for (int kk = 0; kk < width / 16; ++kk) {
+            const uint64_t ad = make_smem_desc(a_s + kk * 32, sbo, swz);
+            const uint64_t bd = make_smem_desc(b_s + kk * 32, sbo, swz);
+            mma_bf16(d_tmem, ad, bd, idesc, (ch > 0 || kk > 0) ? 1u : 0u);
+            issued = true;
+          }
+          mma_commit(smem_u32(&empty_bar[s]));
+        }
+        if (ok) mma_commit(smem_u32(&accf_bar[buf]));
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        flag_error(p.err, kStatusTimeout);
+      }
+      if (!ok && issued) {
+        // wait (bounded) for the MMAs in flight before TMEM is released
+        mma_commit(smem_u32(drain_bar));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(drain_bar), 0))
+          if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;     // accumulator row = weight row of the tile
+    uint32_t li = 0;
+    for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++li) {
+      const Item it = decode_item(w, n_sh, n_tiles, p.shrink);
+      const TileInfo ti = p.tiles[it.tile];
+      const int nmma = (ti.nrows + 15) & ~15;
+      const int buf = li & 1;
+      const bool ok = mbar_wait(smem_u32(&accf_bar[buf]), (li >> 1) & 1, abort_flag);
+      if (bar_red_or(1, 128, !ok || *abort_flag)) {
+        if (!ok) flag_error(p.err, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + buf * TN + (static_cast<uint32_t>(quarter * 32) << 16);
+
+      if (it.shrink) {
+        const ShrinkItem si = p.shrink[it.sh];
+        const int j = row / p.r;
+        const int q = row - j * p.r;
+        const bool valid = j < si.nslot;
+        const int a_j = valid ? p.slot_adapter[si.slot0 + j] : -3;
+        __nv_bfloat16* zrow = p.zbuf + (static_cast<size_t>(si.slot0 + j) * TN) * p.r + q;
+        for (int c0 = 0; c0 < nmma; c0 += 16) {
+          float v[16];
+          tmem_ld16(t_row + c0, v);
+          if (valid) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+              const int c = c0 + cc;
+              const bool keep = c < ti.nrows && p.row_lora[ti.row0 + c] == a_j;
+              zrow[static_cast<size_t>(c) * p.r] = __float2bfloat16_rn(keep ? v[cc] : 0.0f);
+            }
+          }
+        }
+        // publish: every epilogue thread's stores, then one release
+        named_bar_sync(1, 128);
+        if (row == 0) {
+          __threadfence();
+          fence_proxy_async_global();
+          atomicAdd(&p.tile_done[it.tile], 1);
+        }
+      } else if (gate_up) {
+        const bool is_gate = row < 64;
+        const int f = row & 63;
+        const int feat = it.m * 64 + f;
+        __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0) * p.out_ld + feat;
+        for (int c0 = 0; c0 < nmma; c0 += 16) {
+          float v[16];
+          tmem_ld16(t_row + c0, v);
+          if (!is_gate) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) xchg[f * kXchgStride + cc] = v[cc];
+          }
+          named_bar_sync(1, 128);
+          if (is_gate && feat < p.out_feats) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+              const int c = c0 + cc;
+              if (c < ti.nrows) {
+                const float u = xchg[f * kXchgStride + cc];
+                orow[static_cast<size_t>(c) * p.out_ld] = __float2bfloat16_rn(silu_f(v[cc]) * u);
+              }
+            }
+          }
+          named_bar_sync(1, 128);
+        }
+      } else {
+        const int feat = it.m * 128 + row;
+        const bool linear = p.mode == kModeLinear;
+        for (int c0 = 0; c0 < nmma; c0 += 16) {
+          float v[16];
+          tmem_ld16(t_row + c0, v);
+          if (feat < p.out_feats) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+              const int c = c0 + cc;
+              if (c < ti.nrows) {
+                const int prow = ti.row0 + c;
+                if (linear) {
+                  p.out[static_cast<size_t>(p.row_tok[prow]) * p.out_ld + feat] =
+                      __float2bfloat16_rn(v[cc]);
+                } else {
+                  p.out[static_cast<size_t>(prow) * p.out_ld + feat] =
+                      __float2bfloat16_rn(v[cc] * p.row_w[prow]);
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce_bar[buf]));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int TN>
+cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
+  using C = Cfg<TN>;
+  static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<TN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  moe_gemm_kernel<TN><<<grid, kThreads, C::kSmemBytes, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t moe_gemm_smem_bytes(int tn) {
+  return tn >= 256 ? Cfg<256>::kSmemBytes : Cfg<32>::kSmemBytes;
+}
+
+cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
+                            cudaStream_t stream) {
+  if (tn == 256) return launch_tn<256>(maps, p, grid, stream);
+  if (tn == 32) return launch_tn<32>(maps, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moelora

@@ -1,0 +1,54 @@
+// Host-visible declarations of the tcgen05 grouped GEMM (gemm_tc.cu).
+#pragma once
+
+#include <cuda.h>
+#include "common.cuh"
+
+namespace moelora {
+
+enum GemmMode : int { kModeGateUp = 0, kModeDown = 1, kModeLinear = 2 };
+
+// Tensor maps of one GEMM phase.  b[i] / z[i] load 16 << i rows.
+struct alignas(64) GemmMaps {
+  CUtensorMap w;      // base weights, 3D (K, rows, E)
+  CUtensorMap lb;     // LoRA expand weights B, 4D (r, rows, E, L)
+  CUtensorMap la;     // LoRA shrink weights A, 4D (K, r, E, L)
+  CUtensorMap b[5];   // token operand (x_perm or act), 2D (K, rows)
+  CUtensorMap z[5];   // shrink results, 2D (r, slots * tn)
+};
+
+struct GemmParams {
+  int mode;            // GemmMode
+  int K;               // base reduction length
+  int n_mtiles;        // 128-row weight tiles per token tile
+  int out_feats;       // valid output features (I, H or N)
+  int half_rows;       // gate_up: row offset of the `up` half (= I)
+  int r;               // LoRA rank, 0 = no LoRA
+  int lora_w;          // elements of one LoRA K-chunk in shared memory (<= 64)
+  int lora_chunks;     // r / lora_w
+  int lora_swz;        // descriptor layout code of a LoRA chunk
+  int slots_per_item;  // 128 / r
+  int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
+  const WsHeader* hdr;
+  int* err;
+  const TileInfo* tiles;
+  const ShrinkItem* shrink;
+  const int* slot_adapter;
+  const int* row_lora;
+  const float* row_w;
+  const int* row_tok;
+  int* tile_done;
+  __nv_bfloat16* zbuf;  // [slots * tn][r]
+  __nv_bfloat16* out;
+  int out_ld;
+};
+
+// Launches one GEMM phase (shrink items first, then the main items) as a
+// persistent kernel on `grid` CTAs.  tn is 32 or 256.
+cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
+                            cudaStream_t stream);
+
+// Dynamic shared memory of the kernel for a token-tile width.
+size_t moe_gemm_smem_bytes(int tn);
+
+}  // namespace moelora

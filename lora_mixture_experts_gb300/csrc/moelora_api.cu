@@ -1,0 +1,628 @@
+// C ABI of the MoE-LoRA expert layer: argument checks, the workspace plan,
+// TMA tensor maps and the launch sequence
+//   align (hist, scan, scatter) -> permute -> gate_up GEMM phase (with its
+//   LoRA shrink items) -> down GEMM phase (with its shrink items) -> combine
+// all on the caller's stream, with no allocation and no synchronisation.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "align.cuh"
+#include "gemm_tc.cuh"
+
+using namespace moelora;
+
+namespace {
+
+constexpr int kBlockM = 16;          // forward: per-expert row padding = MMA N granularity
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ------------------------------------------------------------ plan
+struct Plan {
+  bool linear = false;
+  int T = 0, k = 0, E = 0, H = 0, I = 0, L = 0, r = 0, N = 0;  // linear: H = K, N = out
+  bool lora = false;
+  int n = 0, nbins = 0, nchunks = 0, block_m = kBlockM, Pmax = 0, tn = 32;
+  int n_tiles_max = 0, n_slots_max = 0, n_sh_max = 0;
+  size_t off_hdr = 0, off_chunk_hist = 0, off_bin_of = 0, off_rank_of = 0, off_bin_start = 0;
+  size_t off_sorted = 0, off_blk = 0, off_seg = 0;
+  size_t off_row_tok = 0, off_row_lora = 0, off_row_w = 0, off_pos_of = 0;
+  size_t off_tiles = 0, off_shrink = 0, off_slot_ad = 0, off_tile_done = 0;
+  size_t off_xperm = 0, off_zgu = 0, off_zd = 0, off_act = 0, off_ypair = 0;
+  size_t total = 0;
+};
+
+struct Bump {
+  size_t cur = 0;
+  size_t take(size_t bytes) {
+    const size_t at = cur;
+    cur = align_up(cur + bytes, kWsAlign);
+    return at;
+  }
+};
+
+bool lora_rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
+
+int check_moe_dims(const moelora_dims* d) {
+  if (!d) return MOELORA_ERR_INVALID_ARG;
+  if (d->T < 0 || d->k < 1 || d->E < 1 || d->k > d->E || d->H < 8 || d->I < 8 || d->L < 0 ||
+      d->r < 0)
+    return MOELORA_ERR_INVALID_ARG;
+  if (d->H % 8 || d->I % 8) return MOELORA_ERR_UNSUPPORTED;
+  const bool lora = d->L > 0 && d->r > 0;
+  if (lora && !lora_rank_ok(d->r)) return MOELORA_ERR_UNSUPPORTED;
+  const int Lp = lora ? d->L + 1 : 1;
+  if (d->E > kMaxExperts || static_cast<long long>(d->E) * Lp > kMaxBins)
+    return MOELORA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->T) * d->k >= (1ll << 30)) return MOELORA_ERR_UNSUPPORTED;
+  return MOELORA_OK;
+}
+
+int check_linear_dims(const moelora_linear_dims* d) {
+  if (!d) return MOELORA_ERR_INVALID_ARG;
+  if (d->T < 0 || d->K < 8 || d->N < 8 || d->L < 0 || d->r < 0) return MOELORA_ERR_INVALID_ARG;
+  if (d->K % 8 || d->N % 8) return MOELORA_ERR_UNSUPPORTED;
+  const bool lora = d->L > 0 && d->r > 0;
+  if (lora && !lora_rank_ok(d->r)) return MOELORA_ERR_UNSUPPORTED;
+  if ((lora ? d->L + 1 : 1) > kMaxBins) return MOELORA_ERR_UNSUPPORTED;
+  if (d->T >= (1 << 30)) return MOELORA_ERR_UNSUPPORTED;
+  return MOELORA_OK;
+}
+
+// Align scratch common to every entry point.
+void plan_align_scratch(Plan& p, Bump& b) {
+  p.n = p.T * p.k;
+  p.nbins = p.E * (p.L + 1);
+  p.nchunks = (p.n + kAlignChunk - 1) / kAlignChunk;
+  p.off_hdr = b.take(sizeof(WsHeader));
+  p.off_chunk_hist = b.take(static_cast<size_t>(p.nchunks) * p.nbins * 4);
+  p.off_bin_of = b.take(static_cast<size_t>(p.n) * 4);
+  p.off_rank_of = b.take(static_cast<size_t>(p.n) * 4);
+  p.off_bin_start = b.take(static_cast<size_t>(p.nbins) * 4);
+}
+
+void plan_gemm_tables(Plan& p, Bump& b) {
+  p.Pmax = p.n + p.E * (p.block_m - 1);
+  const int avg = p.n / p.E;
+  p.tn = avg > 32 ? 256 : 32;
+  p.n_tiles_max = p.n / p.tn + std::min(p.E, std::max(p.n, 1)) + 1;
+  p.n_slots_max = p.lora ? std::min(p.n, p.E * p.L + p.n_tiles_max) : 0;
+  p.n_sh_max = p.n_slots_max;
+  p.off_sorted = b.take(static_cast<size_t>(p.Pmax) * 4);
+  p.off_blk = b.take(static_cast<size_t>(p.Pmax / p.block_m + 1) * 4);
+  p.off_seg = b.take(static_cast<size_t>(p.nbins + 1) * 4);
+  p.off_row_tok = b.take(static_cast<size_t>(p.Pmax) * 4);
+  p.off_row_lora = b.take(static_cast<size_t>(p.Pmax) * 4);
+  p.off_row_w = b.take(static_cast<size_t>(p.Pmax) * 4);
+  p.off_pos_of = b.take(static_cast<size_t>(p.n) * 4);
+  p.off_tiles = b.take(static_cast<size_t>(p.n_tiles_max) * sizeof(TileInfo));
+  p.off_shrink = b.take(static_cast<size_t>(std::max(p.n_sh_max, 1)) * sizeof(ShrinkItem));
+  p.off_slot_ad = b.take(static_cast<size_t>(std::max(p.n_slots_max, 1)) * 4);
+  p.off_tile_done = b.take(static_cast<size_t>(p.n_tiles_max) * 4);
+  p.off_xperm = b.take(static_cast<size_t>(p.Pmax) * p.H * 2);
+  const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
+  p.off_zgu = b.take(std::max<size_t>(zbytes, 16));
+}
+
+Plan plan_forward(const moelora_dims* d) {
+  Plan p;
+  p.T = d->T; p.k = d->k; p.E = d->E; p.H = d->H; p.I = d->I;
+  p.lora = d->L > 0 && d->r > 0;
+  p.L = p.lora ? d->L : 0;
+  p.r = p.lora ? d->r : 0;
+  Bump b;
+  plan_align_scratch(p, b);
+  plan_gemm_tables(p, b);
+  const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
+  p.off_zd = b.take(std::max<size_t>(zbytes, 16));
+  p.off_act = b.take(static_cast<size_t>(p.Pmax) * p.I * 2);
+  p.off_ypair = b.take(static_cast<size_t>(p.Pmax) * p.H * 2);
+  p.total = b.cur;
+  return p;
+}
+
+Plan plan_linear(const moelora_linear_dims* d) {
+  Plan p;
+  p.linear = true;
+  p.T = d->T; p.k = 1; p.E = 1; p.H = d->K; p.I = 0; p.N = d->N;
+  p.lora = d->L > 0 && d->r > 0;
+  p.L = p.lora ? d->L : 0;
+  p.r = p.lora ? d->r : 0;
+  Bump b;
+  plan_align_scratch(p, b);
+  plan_gemm_tables(p, b);
+  p.total = b.cur;
+  return p;
+}
+
+Plan plan_align(const moelora_dims* d) {
+  Plan p;
+  p.T = d->T; p.k = d->k; p.E = d->E;
+  p.L = d->L;   // the align keys on every adapter id in [-1, L)
+  Bump b;
+  plan_align_scratch(p, b);
+  p.total = b.cur;
+  return p;
+}
+
+// ------------------------------------------------------------ device info
+int device_sms() {
+  static std::mutex mu;
+  static int cached_dev = -1;
+  static int cached_sms = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev != cached_dev) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached_dev = dev;
+    cached_sms = sms;
+  }
+  return cached_sms;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for_bytes(int inner_bytes) {
+  if (inner_bytes >= 128) return CU_TENSOR_MAP_SWIZZLE_128B;
+  if (inner_bytes >= 64) return CU_TENSOR_MAP_SWIZZLE_64B;
+  return CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+// bf16 tensor map; dims[0] is the contiguous axis; strides in elements of
+// dims 1.. (converted to bytes here).
+bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_elems, const uint32_t* box) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bdim[5];
+  cuuint32_t estr[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estr[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides_elems[i] * 2;
+  const CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+                           gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle_for_bytes(static_cast<int>(box[0]) * 2),
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS;
+}
+
+bool enc2(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint32_t b0, uint32_t b1) {
+  const uint64_t dims[2] = {d0, d1};
+  const uint64_t str[1] = {d0};
+  const uint32_t box[2] = {b0, b1};
+  return encode_map(m, base, 2, dims, str, box);
+}
+
+bool enc3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+          uint32_t b1) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t str[2] = {d0, d0 * d1};
+  const uint32_t box[3] = {b0, b1, 1};
+  return encode_map(m, base, 3, dims, str, box);
+}
+
+bool enc4(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+          uint32_t b0, uint32_t b1) {
+  const uint64_t dims[4] = {d0, d1, d2, d3};
+  const uint64_t str[3] = {d0, d0 * d1, d0 * d1 * d2};
+  const uint32_t box[4] = {b0, b1, 1, 1};
+  return encode_map(m, base, 4, dims, str, box);
+}
+
+// token-operand and shrink-result maps for every box height up to tn
+bool enc_row_maps(CUtensorMap* maps, const void* base, uint64_t width, uint64_t rows,
+                  uint32_t box_w, int tn) {
+  for (int i = 0; i < 5; ++i) {
+    if ((16 << i) > tn) {
+      std::memset(&maps[i], 0, sizeof(CUtensorMap));
+      continue;
+    }
+    if (!enc2(&maps[i], base, width, rows, box_w, 16u << i)) return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------ launch log / timing hook
+std::mutex g_hook_mu;
+cudaEvent_t g_events[64];
+int g_n_events = 0;
+int g_last_launches = 0;
+const char* g_last_names[32];
+
+struct Launcher {
+  cudaStream_t stream;
+  int count = 0;
+  int n_events = 0;
+  cudaEvent_t events[64];
+  const char* names[32];
+  explicit Launcher(cudaStream_t s) : stream(s) {
+    std::lock_guard<std::mutex> lk(g_hook_mu);
+    n_events = g_n_events;
+    for (int i = 0; i < n_events; ++i) events[i] = g_events[i];
+  }
+  void before(const char* name) {
+    if (count < n_events) cudaEventRecord(events[count], stream);
+    if (count < 32) names[count] = name;
+    ++count;
+  }
+  void finish() {
+    if (count < n_events) cudaEventRecord(events[count], stream);
+    std::lock_guard<std::mutex> lk(g_hook_mu);
+    g_last_launches = count;
+    for (int i = 0; i < count && i < 32; ++i) g_last_names[i] = names[i];
+  }
+};
+
+cudaError_t run_align(Launcher& ln, const AlignArgs& a, cudaStream_t stream) {
+  cudaError_t e;
+  if (a.nchunks > 0) {
+    ln.before("align_hist");
+    if ((e = launch_align_hist(a, stream)) != cudaSuccess) return e;
+  }
+  ln.before("align_scan");
+  if ((e = launch_align_scan(a, stream)) != cudaSuccess) return e;
+  if (a.nchunks > 0) {
+    ln.before("align_scatter");
+    if ((e = launch_align_scatter(a, stream)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
+
+template <typename T>
+T* ws_ptr(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+AlignArgs align_args(const Plan& p, void* ws) {
+  AlignArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.T = p.T; a.k = p.k; a.E = p.E; a.L = p.L;
+  a.n = p.n; a.nbins = p.nbins; a.nchunks = p.nchunks;
+  a.block_m = p.block_m; a.Pmax = p.Pmax;
+  a.chunk_hist = ws_ptr<int>(ws, p.off_chunk_hist);
+  a.bin_of = ws_ptr<int>(ws, p.off_bin_of);
+  a.rank_of = ws_ptr<int>(ws, p.off_rank_of);
+  a.bin_start = ws_ptr<int>(ws, p.off_bin_start);
+  a.hdr = ws_ptr<WsHeader>(ws, p.off_hdr);
+  return a;
+}
+
+void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
+  a.sorted_ids = ws_ptr<int>(ws, p.off_sorted);
+  a.blk_expert = ws_ptr<int>(ws, p.off_blk);
+  a.seg_off = ws_ptr<int>(ws, p.off_seg);
+  a.num_post_pad = nullptr;
+  a.row_tok = ws_ptr<int>(ws, p.off_row_tok);
+  a.row_lora = ws_ptr<int>(ws, p.off_row_lora);
+  a.row_w = ws_ptr<float>(ws, p.off_row_w);
+  a.pos_of = ws_ptr<int>(ws, p.off_pos_of);
+  a.tn = p.tn;
+  a.spi = p.lora ? 128 / p.r : 0;
+  a.tiles = ws_ptr<TileInfo>(ws, p.off_tiles);
+  a.shrink = ws_ptr<ShrinkItem>(ws, p.off_shrink);
+  a.slot_adapter = ws_ptr<int>(ws, p.off_slot_ad);
+  a.tile_done = ws_ptr<int>(ws, p.off_tile_done);
+}
+
+GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
+  GemmParams g;
+  std::memset(&g, 0, sizeof(g));
+  g.r = p.r;
+  g.lora_w = p.lora ? std::min(p.r, 64) : 64;
+  g.lora_chunks = p.lora ? p.r / g.lora_w : 0;
+  g.lora_swz = g.lora_w >= 64 ? 2 : (g.lora_w >= 32 ? 4 : 6);
+  g.slots_per_item = p.lora ? 128 / p.r : 0;
+  g.hdr = a.hdr;
+  g.err = &a.hdr->err;
+  g.tiles = a.tiles;
+  g.shrink = a.shrink;
+  g.slot_adapter = a.slot_adapter;
+  g.row_lora = a.row_lora;
+  g.row_w = a.row_w;
+  g.row_tok = a.row_tok;
+  g.tile_done = a.tile_done;
+  return g;
+}
+
+int gemm_grid(const Plan& p, int n_mtiles, int sms) {
+  const long long items = static_cast<long long>(p.n_sh_max) + static_cast<long long>(p.n_tiles_max) * n_mtiles;
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(items, sms)));
+}
+
+#define MOELORA_CUDA_CHECK(expr)                 \
+  do {                                           \
+    if ((expr) != cudaSuccess) return MOELORA_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t moelora_workspace_bytes(const moelora_dims* d) {
+  if (check_moe_dims(d) != MOELORA_OK) return 0;
+  return plan_forward(d).total;
+}
+
+size_t moelora_linear_workspace_bytes(const moelora_linear_dims* d) {
+  if (check_linear_dims(d) != MOELORA_OK) return 0;
+  return plan_linear(d).total;
+}
+
+size_t moelora_align_workspace_bytes(const moelora_dims* d) {
+  if (!d || d->T < 0 || d->k < 1 || d->E < 1 || d->L < 0) return 0;
+  if (d->E > kMaxExperts || static_cast<long long>(d->E) * (d->L + 1) > kMaxBins) return 0;
+  return plan_align(d).total;
+}
+
+size_t moelora_align_capacity(const moelora_dims* d, int32_t block_m) {
+  if (!d || d->T < 0 || d->k < 1 || d->E < 1 || block_m < 1 || block_m > 1024) return 0;
+  return static_cast<size_t>(d->T) * d->k + static_cast<size_t>(d->E) * (block_m - 1);
+}
+
+int moe_lora_align(const moelora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids,
+                   int32_t block_m, int32_t* sorted_ids, int32_t* blk_expert, int32_t* seg_off,
+                   int32_t* num_post_pad, void* ws, size_t ws_bytes, moelora_stream_t stream_) {
+  if (!d || d->T < 0 || d->k < 1 || d->E < 1 || d->L < 0 || block_m < 1 || block_m > 1024)
+    return MOELORA_ERR_INVALID_ARG;
+  if (d->E > kMaxExperts || static_cast<long long>(d->E) * (d->L + 1) > kMaxBins)
+    return MOELORA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->T) * d->k >= (1ll << 30)) return MOELORA_ERR_UNSUPPORTED;
+  if ((d->T > 0 && (!topk_ids || !lora_ids)) || !sorted_ids || !blk_expert || !seg_off ||
+      !num_post_pad)
+    return MOELORA_ERR_INVALID_ARG;
+  if (!ws) return MOELORA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOELORA_ERR_MISALIGNED;
+  const Plan p = plan_align(d);
+  if (ws_bytes < p.total) return MOELORA_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  AlignArgs a = align_args(p, ws);
+  a.topk_ids = topk_ids;
+  a.lora_ids = lora_ids;
+  a.block_m = block_m;
+  a.Pmax = static_cast<int>(moelora_align_capacity(d, block_m));
+  a.sorted_ids = sorted_ids;
+  a.blk_expert = blk_expert;
+  a.seg_off = seg_off;
+  a.num_post_pad = num_post_pad;
+  Launcher ln(stream);
+  MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
+  MOELORA_CUDA_CHECK(run_align(ln, a, stream));
+  ln.finish();
+  return MOELORA_OK;
+}
+
+int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t* topk_ids,
+                     const float* topk_weights, const int32_t* lora_ids,
+                     const moelora_bf16* W_gate_up, const moelora_bf16* W_down,
+                     const moelora_bf16* A_gu, const moelora_bf16* B_gu, const moelora_bf16* A_d,
+                     const moelora_bf16* B_d, moelora_bf16* out, void* ws, size_t ws_bytes,
+                     moelora_stream_t stream_) {
+  int st = check_moe_dims(d);
+  if (st != MOELORA_OK) return st;
+  if (d->T == 0) return MOELORA_OK;
+  const bool lora = d->L > 0 && d->r > 0;
+  if (!x || !topk_ids || !topk_weights || !lora_ids || !W_gate_up || !W_down || !out)
+    return MOELORA_ERR_INVALID_ARG;
+  if (lora && (!A_gu || !B_gu || !A_d || !B_d)) return MOELORA_ERR_INVALID_ARG;
+  if (misaligned(x) || misaligned(W_gate_up) || misaligned(W_down) || misaligned(out))
+    return MOELORA_ERR_MISALIGNED;
+  if (lora && (misaligned(A_gu) || misaligned(B_gu) || misaligned(A_d) || misaligned(B_d)))
+    return MOELORA_ERR_MISALIGNED;
+  if (!ws) return MOELORA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOELORA_ERR_MISALIGNED;
+  const Plan p = plan_forward(d);
+  if (ws_bytes < p.total) return MOELORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MOELORA_ERR_CUDA;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  AlignArgs a = align_args(p, ws);
+  a.topk_ids = topk_ids;
+  a.lora_ids = lora_ids;
+  a.lora_ignore = p.lora ? 0 : 1;
+  a.topk_weights = topk_weights;
+  fill_gemm_tables(p, ws, a);
+
+  auto* x_perm = ws_ptr<__nv_bfloat16>(ws, p.off_xperm);
+  auto* zgu = ws_ptr<__nv_bfloat16>(ws, p.off_zgu);
+  auto* zd = ws_ptr<__nv_bfloat16>(ws, p.off_zd);
+  auto* act = ws_ptr<__nv_bfloat16>(ws, p.off_act);
+  auto* ypair = ws_ptr<__nv_bfloat16>(ws, p.off_ypair);
+  const uint64_t zrows = static_cast<uint64_t>(std::max(p.n_slots_max, 1)) * p.tn;
+  const uint32_t lw = p.lora ? std::min(p.r, 64) : 64;
+
+  // gate_up phase maps
+  GemmMaps mg;
+  std::memset(&mg, 0, sizeof(mg));
+  bool ok = enc3(&mg.w, W_gate_up, p.H, 2ull * p.I, p.E, 64, 64);
+  ok = ok && enc_row_maps(mg.b, x_perm, p.H, p.Pmax, 64, p.tn);
+  if (p.lora) {
+    ok = ok && enc4(&mg.lb, B_gu, p.r, 2ull * p.I, p.E, p.L, lw, 64);
+    ok = ok && enc4(&mg.la, A_gu, p.H, p.r, p.E, p.L, 64, p.r);
+    ok = ok && enc_row_maps(mg.z, zgu, p.r, zrows, lw, p.tn);
+  }
+  // down phase maps
+  GemmMaps md;
+  std::memset(&md, 0, sizeof(md));
+  ok = ok && enc3(&md.w, W_down, p.I, p.H, p.E, 64, 128);
+  ok = ok && enc_row_maps(md.b, act, p.I, p.Pmax, 64, p.tn);
+  if (p.lora) {
+    ok = ok && enc4(&md.lb, B_d, p.r, p.H, p.E, p.L, lw, 128);
+    ok = ok && enc4(&md.la, A_d, p.I, p.r, p.E, p.L, 64, p.r);
+    ok = ok && enc_row_maps(md.z, zd, p.r, zrows, lw, p.tn);
+  }
+  if (!ok) return MOELORA_ERR_CUDA;
+
+  GemmParams gu = gemm_params(p, ws, a);
+  gu.mode = kModeGateUp;
+  gu.K = p.H;
+  gu.n_mtiles = (p.I + 63) / 64;
+  gu.out_feats = p.I;
+  gu.half_rows = p.I;
+  gu.done_target = 1;
+  gu.zbuf = zgu;
+  gu.out = act;
+  gu.out_ld = p.I;
+
+  GemmParams gd = gemm_params(p, ws, a);
+  gd.mode = kModeDown;
+  gd.K = p.I;
+  gd.n_mtiles = (p.H + 127) / 128;
+  gd.out_feats = p.H;
+  gd.half_rows = 0;
+  gd.done_target = 2;
+  gd.zbuf = zd;
+  gd.out = ypair;
+  gd.out_ld = p.H;
+
+  Launcher ln(stream);
+  MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
+  MOELORA_CUDA_CHECK(run_align(ln, a, stream));
+  ln.before("permute");
+  MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
+                                    p.Pmax, p.H, sms, stream));
+  ln.before("gemm_gate_up");
+  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles, sms), stream));
+  ln.before("gemm_down");
+  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles, sms), stream));
+  ln.before("combine");
+  MOELORA_CUDA_CHECK(launch_combine(ypair, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
+                                    p.k, p.H, sms, stream));
+  ln.finish();
+  return MOELORA_OK;
+}
+
+int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const int32_t* lora_ids,
+                    const moelora_bf16* W, const moelora_bf16* A, const moelora_bf16* B,
+                    moelora_bf16* out, void* ws, size_t ws_bytes, moelora_stream_t stream_) {
+  int st = check_linear_dims(d);
+  if (st != MOELORA_OK) return st;
+  if (d->T == 0) return MOELORA_OK;
+  const bool lora = d->L > 0 && d->r > 0;
+  if (!x || !lora_ids || !W || !out) return MOELORA_ERR_INVALID_ARG;
+  if (lora && (!A || !B)) return MOELORA_ERR_INVALID_ARG;
+  if (misaligned(x) || misaligned(W) || misaligned(out) || (lora && (misaligned(A) || misaligned(B))))
+    return MOELORA_ERR_MISALIGNED;
+  if (!ws) return MOELORA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOELORA_ERR_MISALIGNED;
+  const Plan p = plan_linear(d);
+  if (ws_bytes < p.total) return MOELORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MOELORA_ERR_CUDA;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  AlignArgs a = align_args(p, ws);
+  a.topk_ids = nullptr;     // one expert
+  a.lora_ids = lora_ids;
+  a.lora_ignore = p.lora ? 0 : 1;
+  a.topk_weights = nullptr; // weight 1
+  fill_gemm_tables(p, ws, a);
+  auto* x_perm = ws_ptr<__nv_bfloat16>(ws, p.off_xperm);
+  auto* z = ws_ptr<__nv_bfloat16>(ws, p.off_zgu);
+  const uint64_t zrows = static_cast<uint64_t>(std::max(p.n_slots_max, 1)) * p.tn;
+  const uint32_t lw = p.lora ? std::min(p.r, 64) : 64;
+
+  GemmMaps m;
+  std::memset(&m, 0, sizeof(m));
+  bool ok = enc3(&m.w, W, p.H, p.N, 1, 64, 128);
+  ok = ok && enc_row_maps(m.b, x_perm, p.H, p.Pmax, 64, p.tn);
+  if (p.lora) {
+    ok = ok && enc4(&m.lb, B, p.r, p.N, 1, p.L, lw, 128);
+    ok = ok && enc4(&m.la, A, p.H, p.r, 1, p.L, 64, p.r);
+    ok = ok && enc_row_maps(m.z, z, p.r, zrows, lw, p.tn);
+  }
+  if (!ok) return MOELORA_ERR_CUDA;
+
+  GemmParams g = gemm_params(p, ws, a);
+  g.mode = kModeLinear;
+  g.K = p.H;
+  g.n_mtiles = (p.N + 127) / 128;
+  g.out_feats = p.N;
+  g.done_target = 1;
+  g.zbuf = z;
+  g.out = reinterpret_cast<__nv_bfloat16*>(out);
+  g.out_ld = p.N;
+
+  Launcher ln(stream);
+  MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
+  MOELORA_CUDA_CHECK(run_align(ln, a, stream));
+  ln.before("permute");
+  MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
+                                    p.Pmax, p.H, sms, stream));
+  ln.before("gemm_linear");
+  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, m, g, gemm_grid(p, g.n_mtiles, sms), stream));
+  ln.finish();
+  return MOELORA_OK;
+}
+
+int moelora_set_timing_events(void* const* events, int32_t n_events) {
+  if (n_events < 0 || n_events > 64 || (n_events > 0 && !events)) return MOELORA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_hook_mu);
+  g_n_events = events ? n_events : 0;
+  for (int i = 0; i < g_n_events; ++i) g_events[i] = static_cast<cudaEvent_t>(events[i]);
+  return MOELORA_OK;
+}
+
+int32_t moelora_last_launch_count(void) {
+  std::lock_guard<std::mutex> lk(g_hook_mu);
+  return g_last_launches;
+}
+
+const char* moelora_last_launch_name(int32_t i) {
+  std::lock_guard<std::mutex> lk(g_hook_mu);
+  if (i < 0 || i >= g_last_launches || i >= 32) return "";
+  return g_last_names[i];
+}
+
+int moelora_get_error(void* ws, moelora_stream_t stream) {
+  if (!ws) return MOELORA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOELORA_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpy(&err, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOELORA_ERR_CUDA;
+  return err;
+}
+
+const char* moelora_status_string(int s) {
+  switch (s) {
+    case MOELORA_OK: return "ok";
+    case MOELORA_ERR_INVALID_ARG: return "invalid argument";
+    case MOELORA_ERR_UNSUPPORTED: return "unsupported size";
+    case MOELORA_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case MOELORA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOELORA_ERR_CUDA: return "CUDA error";
+    case MOELORA_ERR_BAD_INDEX: return "expert or adapter id out of range";
+    case MOELORA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,224 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+* align: bit-exact against the oracle's definition for every workload's
+  routing and for edge cases (block_m 1..128, empty experts, all tokens on one
+  expert, adapters absent);
+* forward: the tiny and decode workloads in full; prefill, skewed and the
+  dense linear at full size on sampled tokens the oracle computes one by
+  one; random small shapes with ragged tails (H not a multiple of 128, I not
+  a multiple of 64, T = 1, k = E, every LoRA rank, no LoRA);
+* determinism, CUDA-graph capture/replay, and the device-side bad-index flag.
+"""
+import numpy as np
+import pytest
+import torch
+
+from lora_mixture_experts_gb300 import binding
+from lora_mixture_experts_gb300.inputs import (CONFIGS, DENSE_T_SWEEP, make_linear_case,
+                                               make_moe_case, make_routing, small_moe_case)
+from oracle import moe_lora_ref as ref
+
+from _parity import compare, np_inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _gpu_forward(d, **kw):
+    return binding.moe_lora_forward(d["x"], d["topk_ids"], d["topk_weights"], d["lora_ids"],
+                                    d["W_gate_up"], d["W_down"], d.get("A_gu"), d.get("B_gu"),
+                                    d.get("A_d"), d.get("B_d"), **kw)
+
+
+def _oracle_forward(n, tokens=None):
+    return ref.moe_lora_forward_ref(n["x"], n["topk_ids"], n["topk_weights"], n["lora_ids"],
+                                    n["W_gate_up"], n["W_down"], n.get("A_gu"), n.get("B_gu"),
+                                    n.get("A_d"), n.get("B_d"), tokens=tokens)
+
+
+# ------------------------------------------------------------------ align
+def _check_align(topk_ids, lora_ids, E, L, bm):
+    s, b, seg, npp = binding.moe_lora_align(topk_ids.to(DEV), lora_ids.to(DEV), E, L, bm)
+    torch.cuda.synchronize()
+    exp = ref.align_ref(topk_ids.numpy(), lora_ids.numpy(), E, L, bm)
+    P = exp["num_post_pad"]
+    assert int(npp.item()) == P
+    assert np.array_equal(s[:P].cpu().numpy(), exp["sorted_ids"])
+    assert np.array_equal(b[:P // bm].cpu().numpy(), exp["blk_expert"])
+    assert np.array_equal(seg.cpu().numpy(), exp["seg_off"])
+    n = topk_ids.numel()
+    assert bool((s[P:] == n).all())
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed"])
+@pytest.mark.parametrize("bm", [1, 16, 128])
+def test_align_workloads(name, bm):
+    c = CONFIGS[name]
+    ids, _, lora = make_routing(c, seed=0)
+    _check_align(ids, lora, c.E, c.L, bm)
+
+
+def test_align_edge_cases():
+    g = torch.Generator().manual_seed(3)
+    # all tokens on expert 2 of 5, every adapter -1
+    _check_align(torch.full((37, 1), 2, dtype=torch.int32), torch.full((37,), -1, dtype=torch.int32), 5, 3, 8)
+    # one token
+    _check_align(torch.tensor([[4, 1]], dtype=torch.int32), torch.tensor([0], dtype=torch.int32), 6, 1, 16)
+    # more entries than one align chunk, with empty experts and L = 0
+    ids = torch.randint(0, 3, (700, 2), generator=g, dtype=torch.int32) * 3
+    _check_align(ids, torch.full((700,), -1, dtype=torch.int32), 9, 0, 4)
+    # many bins
+    ids = torch.randint(0, 64, (900, 3), generator=g, dtype=torch.int32)
+    lo = torch.randint(-1, 40, (900,), generator=g, dtype=torch.int32)
+    _check_align(ids, lo, 64, 40, 32)
+
+
+def test_align_bad_index_flag():
+    ids = torch.tensor([[0, 1], [1, 7]], dtype=torch.int32, device=DEV)
+    lo = torch.tensor([0, -1], dtype=torch.int32, device=DEV)
+    d = binding.moelora_dims(2, 2, 4, 8, 8, 2, 0)
+    ws = binding.alloc_workspace(binding.moelora_align_workspace_bytes(d))
+    s, b, seg, npp = binding.moe_lora_align(ids, lo, 4, 2, 4, ws=ws)
+    assert binding.moelora_get_error(ws) == -6
+    assert int(npp.item()) == 12          # three valid entries on experts 0, 1, 1
+
+
+# ------------------------------------------------------------------ forward
+def _run_parity(d, tokens=None, what=""):
+    out = _gpu_forward(d)
+    torch.cuda.synchronize()
+    n = np_inputs(d, lazy=tokens is not None)
+    exp = _oracle_forward(n, tokens)
+    got = out if tokens is None else out[torch.as_tensor(tokens, device=out.device)]
+    ok, msg = compare(got, exp, what)
+    assert ok, msg
+    return out
+
+
+def test_forward_tiny():
+    d = make_moe_case(CONFIGS["tiny"], seed=0, device=DEV)
+    _run_parity(d, what="tiny")
+
+
+def test_forward_decode():
+    d = make_moe_case(CONFIGS["decode"], seed=0, device=DEV)
+    _run_parity(d, what="decode")
+
+
+def test_forward_prefill_sampled():
+    d = make_moe_case(CONFIGS["prefill"], seed=0, device=DEV)
+    rng = np.random.default_rng(0)
+    tokens = np.sort(rng.choice(4096, size=24, replace=False))
+    tokens[0], tokens[-1] = 0, 4095
+    _run_parity(d, tokens=tokens, what="prefill sample")
+
+
+def test_forward_skewed_sampled():
+    d = make_moe_case(CONFIGS["skewed"], seed=0, device=DEV)
+    rng = np.random.default_rng(1)
+    tokens = np.sort(rng.choice(256, size=12, replace=False))
+    _run_parity(d, tokens=tokens, what="skewed sample")
+
+
+SMALL = [
+    # T, H, I, E, k, L, r
+    (1, 64, 64, 1, 1, 1, 16),
+    (5, 136, 72, 3, 2, 2, 16),       # H % 128 != 0, I % 64 != 0
+    (33, 256, 192, 4, 4, 3, 32),     # k == E
+    (70, 128, 128, 6, 2, 5, 64),
+    (19, 192, 320, 5, 3, 2, 128),
+    (40, 200, 136, 7, 2, 0, 0),      # no LoRA
+    (300, 264, 264, 8, 2, 4, 16),    # several tiles per expert, ragged tail
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[f"T{s[0]}_H{s[1]}_I{s[2]}_E{s[3]}_k{s[4]}_L{s[5]}_r{s[6]}" for s in SMALL])
+def test_forward_small_shapes(shape):
+    T, H, I, E, k, L, r = shape
+    c = small_moe_case(T, H, I, E, k, L, r, adapters="uniform_with_none" if L else "uniform")
+    if L == 0:
+        c = small_moe_case(T, H, I, E, k, 1, 16)
+    d = make_moe_case(c, seed=11, device=DEV, lora=L > 0)
+    if L == 0:
+        d["lora_ids"] = torch.full((T,), -1, dtype=torch.int32, device=DEV)
+    _run_parity(d, what=str(shape))
+
+
+def test_forward_all_one_expert_and_no_adapter():
+    c = small_moe_case(200, 128, 128, 4, 1, 3, 32)
+    d = make_moe_case(c, seed=5, device=DEV)
+    d["topk_ids"] = torch.full((200, 1), 3, dtype=torch.int32, device=DEV)
+    d["topk_weights"] = torch.ones((200, 1), dtype=torch.float32, device=DEV)
+    _run_parity(d, what="one expert")
+    d["lora_ids"] = torch.full((200,), -1, dtype=torch.int32, device=DEV)
+    _run_parity(d, what="one expert, no adapters")
+
+
+def test_forward_deterministic_and_graph_capturable():
+    d = make_moe_case(CONFIGS["tiny"], seed=2, device=DEV)
+    dims = binding.dims_of(d["x"], d["topk_ids"], d["W_gate_up"], d["W_down"], d["A_gu"])
+    ws = binding.alloc_workspace(binding.moelora_workspace_bytes(dims))
+    a = _gpu_forward(d, ws=ws).clone()
+    b = _gpu_forward(d, ws=ws).clone()
+    assert torch.equal(a, b)
+    out = torch.empty_like(a)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _gpu_forward(d, ws=ws, out=out)       # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        _gpu_forward(d, ws=ws, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, a)
+
+
+def test_forward_bad_index_flag():
+    d = make_moe_case(CONFIGS["tiny"], seed=0, device=DEV)
+    dims = binding.dims_of(d["x"], d["topk_ids"], d["W_gate_up"], d["W_down"], d["A_gu"])
+    ws = binding.alloc_workspace(binding.moelora_workspace_bytes(dims))
+    _gpu_forward(d, ws=ws)
+    assert binding.moelora_get_error(ws) == 0
+    bad = dict(d, lora_ids=d["lora_ids"].clone())
+    bad["lora_ids"][5] = 9
+    _gpu_forward(bad, ws=ws)
+    assert binding.moelora_get_error(ws) == -6
+    _gpu_forward(d, ws=ws)
+    assert binding.moelora_get_error(ws) == 0
+
+
+# ------------------------------------------------------------------ dense linear
+@pytest.mark.parametrize("T", DENSE_T_SWEEP)
+def test_linear_dense(T):
+    c = CONFIGS[f"dense_t{T}"]
+    d = make_linear_case(c, seed=0, device=DEV)
+    out = binding.moe_lora_linear(d["x"], d["lora_ids"], d["W"], d["A"], d["B"])
+    torch.cuda.synchronize()
+    tokens = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(2).choice(T, 16, replace=False))
+    x = np_inputs({"x": d["x"]})["x"][tokens]
+    lo = d["lora_ids"].cpu().numpy()[tokens]
+    W = np_inputs({"W": d["W"]})["W"]
+    A = np_inputs({"A": d["A"]})["A"]
+    B = np_inputs({"B": d["B"]})["B"]
+    exp = ref.moe_lora_linear_ref(x, lo, W, A, B)
+    ok, msg = compare(out[torch.as_tensor(tokens, device=DEV)], exp, f"dense T={T}")
+    assert ok, msg
+
+
+def test_linear_small_no_lora_and_ragged():
+    g = torch.Generator(device=DEV).manual_seed(4)
+    for (T, K, N, L, r) in [(3, 64, 136, 0, 0), (45, 200, 264, 3, 32), (260, 128, 128, 2, 64)]:
+        x = torch.randn(T, K, generator=g, device=DEV).bfloat16()
+        W = (torch.randn(N, K, generator=g, device=DEV) * K ** -0.5).bfloat16()
+        A = (torch.randn(L, r, K, generator=g, device=DEV) * K ** -0.5).bfloat16() if L else None
+        B = (torch.randn(L, N, r, generator=g, device=DEV) * r ** -0.5).bfloat16() if L else None
+        lo = (torch.randint(-1, L, (T,), generator=g, device=DEV) if L else torch.full((T,), -1, device=DEV)).int()
+        out = binding.moe_lora_linear(x, lo, W, A, B)
+        n = np_inputs({"x": x, "W": W, **({"A": A, "B": B} if L else {})})
+        exp = ref.moe_lora_linear_ref(n["x"], lo.cpu().numpy(), n["W"], n.get("A"), n.get("B"))
+        ok, msg = compare(out, exp, f"linear {(T, K, N, L, r)}")
+        assert ok, msg
