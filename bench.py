@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE-LoRA expert layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config decode|prefill|skewed|tiny|dense_t1|...]
+
+One step = one call of the whole layer (align, permute, gate_up GEMM with
+its LoRA shrink/expand, down GEMM with its LoRA, combine) on one batch of
+seeded synthetic input.  The default workload is the decode batch (T=16,
+H=I=2880, 32 experts top-4, 8 adapters of rank 32); its weights (1.6 GB) are
+larger than the 129 MB L2, so no flush is needed between steps.
+
+Under torchrun every rank runs an independent replica on its own GPU with
+its own batch (no collective on the data path); the timed region is
+bracketed by a barrier and a synchronize, and the slowest rank's time
+counts.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (float64 numpy) on this host's cores
+on a bounded sample of the same workload; only rank 0 works under torchrun.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-LoRA layer routed tokens/s; % of HBM (decode) / bf16 TC (prefill) roofline"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="bounded CPU work of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", index, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [v.strip() for v in line.split(",")]))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.01)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        note = "inside timed region"
+        if not inside and self.samples:
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:2]
+            inside = [s for _, s in near]
+            note = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        mx = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 4 + i and s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# --------------------------------------------------------------- helpers
+def reduce_max(v: float, world: int, device) -> float:
+    """The slowest rank's figure (every rank gets it); a no-op on one rank."""
+    if world <= 1:
+        return v
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each replica draws its own batch (weights and routing) from its rank."""
+    return rank
+
+
+def workload_name(c):
+    from lora_mixture_experts_gb300.inputs import LinearCase
+    if isinstance(c, LinearCase):
+        return (f"{c.name}: dense multi-LoRA linear x[{c.T},{c.K}] @ W[{c.N},{c.K}]^T + LoRA "
+                f"r={c.r} over {c.L} adapters")
+    return (f"{c.name}: T={c.T}, H={c.H}, I={c.I}, E={c.E}, top-{c.k}, {c.L} adapters r={c.r}, "
+            f"routing={c.routing}, adapters={c.adapters}")
+
+
+def source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "lora_mixture_experts_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(config_name, kernel):
+    """DRAM bytes per launch of `kernel` from a committed ncu capture, if the
+    kernel sources have not changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(config_name, {}).get(kernel)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def oracle_baseline(case, host, seconds, tokens=None):
+    """Times the oracle on this host on a bounded sample; returns (tokens/s, sample text)."""
+    from oracle import moe_lora_ref as ref
+    from lora_mixture_experts_gb300.inputs import LinearCase
+    T = case.T
+    if tokens is None:
+        tokens = list(range(T))
+    n_done = 0
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        if isinstance(case, LinearCase):
+            ref.moe_lora_linear_ref(host["x"][tokens], host["lora_ids"][tokens], host["W"],
+                                    host["A"], host["B"])
+        else:
+            ref.moe_lora_forward_ref(host["x"], host["topk_ids"], host["topk_weights"],
+                                     host["lora_ids"], host["W_gate_up"], host["W_down"],
+                                     host.get("A_gu"), host.get("B_gu"), host.get("A_d"),
+                                     host.get("B_d"), tokens=tokens)
+        n_done += len(tokens)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    sample = (f"{len(tokens)} of {T} tokens of the {case.name} batch per oracle call, "
+              f"{reps} calls in {el:.1f} s")
+    return n_done / el, sample
+
+
+def host_inputs(d):
+    from lora_mixture_experts_gb300.inputs import bf16_bits
+    import torch
+    out = {}
+    for k, v in d.items():
+        out[k] = bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()
+    return out
+
+
+def sample_tokens(case, budget_tokens):
+    import numpy as np
+    if case.T <= budget_tokens:
+        return list(range(case.T))
+    rng = np.random.default_rng(0)
+    return sorted(rng.choice(case.T, size=budget_tokens, replace=False).tolist())
+
+
+def oracle_budget_tokens(case):
+    # tokens per oracle call: the whole batch when it is small, else a sample
+    # that keeps one call around a second
+    from lora_mixture_experts_gb300.inputs import LinearCase
+    if isinstance(case, LinearCase):
+        return min(case.T, 64)
+    return min(case.T, 64 if case.H * case.I <= 2880 * 2880 else 16)
+
+
+# --------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    from lora_mixture_experts_gb300.inputs import CONFIGS, LinearCase, make_linear_case, make_moe_case
+    if rank != 0:
+        return None
+    case = CONFIGS[args.config]
+    d = make_linear_case(case, 0, "cpu") if isinstance(case, LinearCase) else make_moe_case(case, 0, "cpu")
+    host = host_inputs(d)
+    tokens = sample_tokens(case, oracle_budget_tokens(case))
+    from oracle import moe_lora_ref as ref
+    for _ in range(max(args.warmup, 0)):
+        oracle_baseline(case, host, 0.0, tokens)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_baseline(case, host, 0.0, tokens)
+        times.append(time.perf_counter() - t0)
+    el = sum(times)
+    value = len(tokens) * args.steps / el
+    sample = f"{len(tokens)} of {case.T} tokens of the {case.name} batch per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(case), "parallelism": "host CPU (oracle)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import numpy as np
+    from lora_mixture_experts_gb300 import binding, roofline
+    from lora_mixture_experts_gb300.inputs import CONFIGS, LinearCase, make_linear_case, make_moe_case
+
+    binding.load(build_if_missing=True)
+    case = CONFIGS[args.config]
+    linear = isinstance(case, LinearCase)
+    seed = rank_seed(rank)
+    d = make_linear_case(case, seed=seed, device=device) if linear else make_moe_case(case, seed=seed, device=device)
+    peaks = roofline.load_peaks(ROOT)
+
+    if linear:
+        dims = binding.moelora_linear_dims(case.T, case.K, case.N, case.L, case.r)
+        ws = binding.alloc_workspace(binding.moelora_linear_workspace_bytes(dims), device)
+        out = torch.empty((case.T, case.N), dtype=torch.bfloat16, device=device)
+
+        def fwd(x=d["x"], lo=d["lora_ids"]):
+            binding.moe_lora_linear(x, lo, d["W"], d["A"], d["B"], out=out, ws=ws)
+        lo_np = d["lora_ids"].cpu().numpy()
+        layer = roofline.linear_work(lo_np, case.K, case.N, case.r)
+        kernel_work = {"gemm_linear": layer}
+        step_inputs = ["x", "lora_ids"]
+    else:
+        dims = binding.dims_of(d["x"], d["topk_ids"], d["W_gate_up"], d["W_down"], d["A_gu"])
+        ws = binding.alloc_workspace(binding.moelora_workspace_bytes(dims), device)
+        out = torch.empty_like(d["x"])
+
+        def fwd(x=d["x"], ids=d["topk_ids"], w=d["topk_weights"], lo=d["lora_ids"]):
+            binding.moe_lora_forward(x, ids, w, lo, d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"],
+                                     d["A_d"], d["B_d"], out=out, ws=ws)
+        layer, gu, dn = roofline.moe_layer_work(d["topk_ids"].cpu().numpy(), d["lora_ids"].cpu().numpy(),
+                                                case.H, case.I, case.r)
+        kernel_work = {"gemm_gate_up": gu, "gemm_down": dn}
+        step_inputs = ["x", "topk_ids", "topk_weights", "lora_ids"]
+
+    stream = torch.cuda.current_stream()
+    fwd()
+    torch.cuda.synchronize()
+    status = binding.moelora_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {binding.moelora_status_string(status)}")
+    names = binding.moelora_last_launches()
+    nl = len(names)
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(K)]
+    for row in ev:                      # create the events before the timed region
+        for e in row:
+            e.record()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    dev_index = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[device.index] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(device.index)
+    sampler = ClockSampler(dev_index)
+    sampler.wait_first()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record()
+    for i in range(K):
+        binding.moelora_set_timing_events(ev[i])
+        fwd()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    binding.moelora_set_timing_events(None)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1) / K
+    sampler_summary = sampler.summary(t_wall0, t_wall1)
+    sampler.stop()
+    ms = reduce_max(ms, world, device)
+
+    # per-kernel device time over the timed steps
+    per = {}
+    for i in range(K):
+        for j in range(nl):
+            per.setdefault(names[j], []).append(ev[i][j].elapsed_time(ev[i][j + 1]))
+    kernel_ms = {n: sum(v) / len(v) for n, v in per.items()}
+    dom = max(kernel_work, key=lambda n: kernel_ms.get(n, 0.0))
+    w = kernel_work[dom]
+    sustained = True
+    bound = roofline.bound_of(w, peaks, sustained)
+    dur_s = kernel_ms[dom] / 1e3
+    if bound == "hbm":
+        achieved, peak, unit = w.bytes / dur_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = w.flops / dur_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    traffic = load_traffic(args.config, dom)
+
+    # end to end through the public API: inputs from pinned host memory,
+    # result read back, every step
+    host = {k: d[k].cpu().pin_memory() for k in step_inputs}
+    dev_in = {k: torch.empty_like(d[k]) for k in step_inputs}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        for k in step_inputs:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        fwd(*[dev_in[k] for k in step_inputs])
+        out_h.copy_(out, non_blocking=True)
+    for _ in range(min(args.warmup, 5)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / K
+    e2e_s = reduce_max(e2e_s, world, device)
+
+    T = case.T
+    value = T * world / (ms / 1e3)
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(case), "tokens_per_step_per_gpu": T,
+                   "l2": "weights larger than the 129 MB L2, no flush between steps",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peaks['source']} ({'bf16 sustained' if unit == 'TFLOP/s' else 'HBM copy'})",
+                     "algorithmic_bytes": w.bytes, "algorithmic_flops": w.flops,
+                     "kernel_ms": kernel_ms[dom]},
+        "layer_roofline": {"bound": roofline.bound_of(layer, peaks, sustained),
+                           "t_roof_ms": 1e3 * roofline.roofline_time_s(layer, peaks, sustained),
+                           "frac": 1e3 * roofline.roofline_time_s(layer, peaks, sustained) / ms,
+                           "bytes": layer.bytes, "flops": layer.flops},
+        "kernel_ms": kernel_ms,
+        "e2e": {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": nl * K,
+        "clocks": sampler_summary,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        hostw = host_inputs({k: v for k, v in d.items()})
+        tokens = sample_tokens(case, oracle_budget_tokens(case))
+        v, sample = oracle_baseline(case, hostw, args.cpu_seconds, tokens)
+        res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                               "sample": sample}
+    return res
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    import torch
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        res = run_ours(args, rank, world, device)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

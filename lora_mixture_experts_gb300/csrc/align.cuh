@@ -58,7 +58,7 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bflo
                            int Pmax, int H, int num_sms, cudaStream_t stream);
 
 // out[t] = sum_j y_pair[pos_of[t*k+j]] in fp32, j ascending, one bf16 rounding.
-cudaError_t launch_combine(const __nv_bfloat16* y_pair, const int* pos_of, __nv_bfloat16* out,
+cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
                            int T, int k, int H, int num_sms, cudaStream_t stream);
 
 }  // namespace moelora

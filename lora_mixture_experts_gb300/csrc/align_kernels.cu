@@ -244,32 +244,28 @@ __global__ void permute_kernel(const uint4* __restrict__ x, const int* __restric
   }
 }
 
-__global__ void combine_kernel(const uint4* __restrict__ y_pair, const int* __restrict__ pos_of,
-                               uint4* __restrict__ out, int T, int k, int hv) {
+__global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __restrict__ pos_of,
+                               uint2* __restrict__ out, int T, int k, int hv) {
+  // hv = H / 4: four features per thread
   const size_t total = static_cast<size_t>(T) * hv;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(i / hv);
     const int c = static_cast<int>(i - static_cast<size_t>(t) * hv);
-    float acc[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const int pos = pos_of[t * k + j];
       if (pos < 0) continue;
-      const uint4 v = y_pair[static_cast<size_t>(pos) * hv + c];
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f2 = __bfloat1622float2(h2[q]);
-        acc[2 * q] += f2.x;
-        acc[2 * q + 1] += f2.y;
-      }
+      const float4 v = y_pair[static_cast<size_t>(pos) * hv + c];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
     }
-    uint4 o;
+    uint2 o;
     __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) o2[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    o2[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    o2[1] = __floats2bfloat162_rn(acc.z, acc.w);
     out[i] = o;
   }
 }
@@ -304,14 +300,14 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bflo
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const __nv_bfloat16* y_pair, const int* pos_of, __nv_bfloat16* out,
+cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
                            int T, int k, int H, int num_sms, cudaStream_t stream) {
-  const int hv = H / 8;
+  const int hv = H / 4;
   const size_t total = static_cast<size_t>(T) * hv;
   int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
   if (grid < 1) grid = 1;
-  combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(y_pair), pos_of,
-                                           reinterpret_cast<uint4*>(out), T, k, hv);
+  combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(y_pair), pos_of,
+                                           reinterpret_cast<uint2*>(out), T, k, hv);
   return cudaGetLastError();
 }
 

@@ -11,8 +11,9 @@
 //  * main items    -- a 128-row tile of the expert's weight rows against one
 //    token tile: acc = W_tile X^T (K loop over the hidden size) followed by
 //    one K-chunk of width r per adapter present: acc += B[a,e]_tile Z_a^T.
-//    The epilogue applies SiLU(gate)*up (gate_up), the gate weight (down) or
-//    nothing (dense linear) and stores bf16.
+//    The epilogue applies SiLU(gate)*up (gate_up, stored bf16), the gate
+//    weight (down, stored fp32 for the combine) or nothing (dense linear,
+//    stored bf16).
 //
 // Orientation: the weight rows are the MMA's M side (128 rows) and the
 // tokens its N side (16..256, rounded up to 16), so a decode-sized tile with
@@ -373,8 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   p.out[static_cast<size_t>(p.row_tok[prow]) * p.out_ld + feat] =
                       __float2bfloat16_rn(v[cc]);
                 } else {
-                  p.out[static_cast<size_t>(prow) * p.out_ld + feat] =
-                      __float2bfloat16_rn(v[cc] * p.row_w[prow]);
+                  p.out_f32[static_cast<size_t>(prow) * p.out_ld + feat] = v[cc] * p.row_w[prow];
                 }
               }
             }

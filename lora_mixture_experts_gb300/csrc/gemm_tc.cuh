@@ -39,7 +39,8 @@ struct GemmParams {
   const int* row_tok;
   int* tile_done;
   __nv_bfloat16* zbuf;  // [slots * tn][r]
-  __nv_bfloat16* out;
+  __nv_bfloat16* out;   // act [Pmax][I] (gate_up) or out [T][N] (linear)
+  float* out_f32;       // y_pair [Pmax][H] (down): gate-weighted expert output, fp32
   int out_ld;
 };
 

@@ -121,7 +121,7 @@ Plan plan_forward(const moelora_dims* d) {
   const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
   p.off_zd = b.take(std::max<size_t>(zbytes, 16));
   p.off_act = b.take(static_cast<size_t>(p.Pmax) * p.I * 2);
-  p.off_ypair = b.take(static_cast<size_t>(p.Pmax) * p.H * 2);
+  p.off_ypair = b.take(static_cast<size_t>(p.Pmax) * p.H * 4);
   p.total = b.cur;
   return p;
 }
@@ -454,7 +454,7 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   auto* zgu = ws_ptr<__nv_bfloat16>(ws, p.off_zgu);
   auto* zd = ws_ptr<__nv_bfloat16>(ws, p.off_zd);
   auto* act = ws_ptr<__nv_bfloat16>(ws, p.off_act);
-  auto* ypair = ws_ptr<__nv_bfloat16>(ws, p.off_ypair);
+  auto* ypair = ws_ptr<float>(ws, p.off_ypair);
   const uint64_t zrows = static_cast<uint64_t>(std::max(p.n_slots_max, 1)) * p.tn;
   const uint32_t lw = p.lora ? std::min(p.r, 64) : 64;
 
@@ -499,7 +499,8 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   gd.half_rows = 0;
   gd.done_target = 2;
   gd.zbuf = zd;
-  gd.out = ypair;
+  gd.out = nullptr;
+  gd.out_f32 = ypair;
   gd.out_ld = p.H;
 
   Launcher ln(stream);
