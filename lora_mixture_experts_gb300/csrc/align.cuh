@@ -48,10 +48,11 @@ struct AlignArgs {
 };
 
 // The three align kernels; hist and scatter are skipped (return success)
-// when there are no entries.
-cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream);
-cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream);
-cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream);
+// when there are no entries.  `chained`: the launch may overlap the tail of
+// the preceding kernel on the stream (programmatic dependent launch).
+cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream, bool chained);
+cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream, bool chained);
+cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained);
 
 // x_perm[p] = x[row_tok[p]] (zero rows for padding), p < Pmax.
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,

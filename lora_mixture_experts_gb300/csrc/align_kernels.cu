@@ -21,6 +21,8 @@ namespace {
 constexpr int kScanThreads = 1024;
 
 __global__ void __launch_bounds__(kAlignChunk) align_hist_kernel(AlignArgs a) {
+  grid_dependency_wait();
+  grid_dependency_trigger();
   __shared__ int bins[kAlignChunk];
   extern __shared__ int hist[];   // [nbins]
   const int c = blockIdx.x;
@@ -80,6 +82,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
   __shared__ int warp_sums[32];
+  grid_dependency_wait();
+  grid_dependency_trigger();
   const int tid = threadIdx.x;
   const int Lp = a.L + 1;
 
@@ -213,6 +217,8 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
 }
 
 __global__ void __launch_bounds__(kAlignChunk) align_scatter_kernel(AlignArgs a) {
+  grid_dependency_wait();
+  grid_dependency_trigger();
   const int c = blockIdx.x;
   const int f = c * kAlignChunk + threadIdx.x;
   if (f >= a.n) return;
@@ -234,6 +240,8 @@ __global__ void __launch_bounds__(kAlignChunk) align_scatter_kernel(AlignArgs a)
 
 __global__ void permute_kernel(const uint4* __restrict__ x, const int* __restrict__ row_tok,
                                uint4* __restrict__ x_perm, int Pmax, int hv) {
+  grid_dependency_wait();
+  grid_dependency_trigger();
   const size_t total = static_cast<size_t>(Pmax) * hv;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -247,6 +255,8 @@ __global__ void permute_kernel(const uint4* __restrict__ x, const int* __restric
 __global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __restrict__ pos_of,
                                uint2* __restrict__ out, int T, int k, int hv) {
   // hv = H / 4: four features per thread
+  grid_dependency_wait();
+  grid_dependency_trigger();
   const size_t total = static_cast<size_t>(T) * hv;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -272,21 +282,20 @@ __global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __r
 
 }  // namespace
 
-cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream) {
+cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream, bool chained) {
   if (a.nchunks == 0) return cudaSuccess;
-  align_hist_kernel<<<a.nchunks, kAlignChunk, a.nbins * sizeof(int), stream>>>(a);
-  return cudaGetLastError();
+  return launch_chained(align_hist_kernel, dim3(a.nchunks), dim3(kAlignChunk),
+                        a.nbins * sizeof(int), stream, chained, a);
 }
 
-cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream) {
-  align_scan_kernel<<<1, kScanThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream, bool chained) {
+  return launch_chained(align_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, chained, a);
 }
 
-cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream) {
+cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained) {
   if (a.nchunks == 0) return cudaSuccess;
-  align_scatter_kernel<<<a.nchunks, kAlignChunk, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_chained(align_scatter_kernel, dim3(a.nchunks), dim3(kAlignChunk), 0, stream,
+                        chained, a);
 }
 
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
@@ -295,9 +304,9 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bflo
   const size_t total = static_cast<size_t>(Pmax) * hv;
   int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
   if (grid < 1) grid = 1;
-  permute_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), row_tok,
-                                           reinterpret_cast<uint4*>(x_perm), Pmax, hv);
-  return cudaGetLastError();
+  return launch_chained(permute_kernel, dim3(grid), dim3(256), 0, stream, true,
+                        reinterpret_cast<const uint4*>(x), row_tok, reinterpret_cast<uint4*>(x_perm),
+                        Pmax, hv);
 }
 
 cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
@@ -306,9 +315,9 @@ cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16
   const size_t total = static_cast<size_t>(T) * hv;
   int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
   if (grid < 1) grid = 1;
-  combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(y_pair), pos_of,
-                                           reinterpret_cast<uint2*>(out), T, k, hv);
-  return cudaGetLastError();
+  return launch_chained(combine_kernel, dim3(grid), dim3(256), 0, stream, true,
+                        reinterpret_cast<const float4*>(y_pair), pos_of, reinterpret_cast<uint2*>(out),
+                        T, k, hv);
 }
 
 }  // namespace moelora

@@ -49,6 +49,36 @@ __device__ __forceinline__ void flag_error(int* err, int code) {
   atomicCAS(err, 0, code);
 }
 
+// ---------------------------------------------------------------- launch chaining
+// Programmatic dependent launch: every kernel of the layer waits for the
+// preceding kernel's results before reading them and then allows the next
+// kernel to begin launching.  Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host side: launch `kernel` on `stream`, allowed to overlap the preceding
+// kernel's tail when `chained` (the kernel must call grid_dependency_wait()
+// before reading that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, bool chained, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = chained ? attr : nullptr;
+  cfg.numAttrs = chained ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- timing
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

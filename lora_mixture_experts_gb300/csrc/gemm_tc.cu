@@ -55,7 +55,14 @@ struct Item {
   int sh;       // shrink item index
 };
 
-__device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, const ShrinkItem* sh) {
+// Item order: all shrink items first, then the main items in groups of
+// `gt` consecutive token tiles.  Inside a group the weight tile m is the
+// slow index and the tile the fast one, so the tiles of one expert (adjacent
+// in the tile table) share each weight tile through L2 while it is hot, and
+// the group's token rows (sized by the host to a fraction of L2) stay
+// resident across all m.
+__device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_m, int gt,
+                                            const ShrinkItem* sh) {
   Item it;
   if (w < n_sh) {
     it.shrink = 1;
@@ -64,10 +71,15 @@ __device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, const 
     it.m = 0;
   } else {
     w -= n_sh;
+    const int per_group = gt * n_m;
+    const int g = w / per_group;
+    const int wl = w - g * per_group;
+    const int t0 = g * gt;
+    const int ntg = min(gt, n_tiles - t0);
     it.shrink = 0;
     it.sh = -1;
-    it.tile = w % n_tiles;
-    it.m = w / n_tiles;
+    it.m = wl / ntg;
+    it.tile = t0 + (wl - it.m * ntg);
   }
   return it;
 }
@@ -133,6 +145,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+  // results of the preceding launch (x_perm / act, the tile tables) are read
+  // only after this point; the next launch may start its own preamble
+  grid_dependency_wait();
+  grid_dependency_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -150,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const Item it = decode_item(w, n_sh, n_tiles, p.shrink);
+        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
         const TileInfo ti = p.tiles[it.tile];
         const int nmma = (ti.nrows + 15) & ~15;
         const int bi = box_index(nmma);
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool issued = false;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++li) {
-        const Item it = decode_item(w, n_sh, n_tiles, p.shrink);
+        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
         const TileInfo ti = p.tiles[it.tile];
         const int nmma = (ti.nrows + 15) & ~15;
         const uint32_t idesc = make_idesc_bf16(nmma);
@@ -294,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;     // accumulator row = weight row of the tile
     uint32_t li = 0;
     for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++li) {
-      const Item it = decode_item(w, n_sh, n_tiles, p.shrink);
+      const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
       const TileInfo ti = p.tiles[it.tile];
       const int nmma = (ti.nrows + 15) & ~15;
       const int buf = li & 1;
@@ -408,8 +424,8 @@ cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaS
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  moe_gemm_kernel<TN><<<grid, kThreads, C::kSmemBytes, stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_chained(moe_gemm_kernel<TN>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream,
+                        true, maps, p);
 }
 
 }  // namespace

@@ -29,6 +29,7 @@ struct GemmParams {
   int lora_swz;        // descriptor layout code of a LoRA chunk
   int slots_per_item;  // 128 / r
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
+  int group_tiles;     // token tiles per L2 group of the main-item order
   const WsHeader* hdr;
   int* err;
   const TileInfo* tiles;

@@ -278,19 +278,28 @@ struct Launcher {
   }
 };
 
+// The align kernels; the first one follows a memset and is not chained.
 cudaError_t run_align(Launcher& ln, const AlignArgs& a, cudaStream_t stream) {
   cudaError_t e;
+  bool first = true;
   if (a.nchunks > 0) {
     ln.before("align_hist");
-    if ((e = launch_align_hist(a, stream)) != cudaSuccess) return e;
+    if ((e = launch_align_hist(a, stream, !first)) != cudaSuccess) return e;
+    first = false;
   }
   ln.before("align_scan");
-  if ((e = launch_align_scan(a, stream)) != cudaSuccess) return e;
+  if ((e = launch_align_scan(a, stream, !first)) != cudaSuccess) return e;
   if (a.nchunks > 0) {
     ln.before("align_scatter");
-    if ((e = launch_align_scatter(a, stream)) != cudaSuccess) return e;
+    if ((e = launch_align_scatter(a, stream, true)) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Token tiles per L2 group: the group's token rows take about 32 MB of L2.
+int group_tiles(int tn, int K) {
+  const long long per_tile = static_cast<long long>(tn) * K * 2;
+  return static_cast<int>(std::max<long long>(1, (32ll << 20) / per_tile));
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
@@ -487,6 +496,7 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   gu.out_feats = p.I;
   gu.half_rows = p.I;
   gu.done_target = 1;
+  gu.group_tiles = group_tiles(p.tn, p.H);
   gu.zbuf = zgu;
   gu.out = act;
   gu.out_ld = p.I;
@@ -498,6 +508,7 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   gd.out_feats = p.H;
   gd.half_rows = 0;
   gd.done_target = 2;
+  gd.group_tiles = group_tiles(p.tn, p.I);
   gd.zbuf = zd;
   gd.out = nullptr;
   gd.out_f32 = ypair;
@@ -567,6 +578,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   g.n_mtiles = (p.N + 127) / 128;
   g.out_feats = p.N;
   g.done_target = 1;
+  g.group_tiles = group_tiles(p.tn, p.H);
   g.zbuf = z;
   g.out = reinterpret_cast<__nv_bfloat16*>(out);
   g.out_ld = p.N;
