@@ -15,7 +15,8 @@
  * Conventions for every entry point:
  *  - Pointers named *_dev are DEVICE pointers on the current CUDA device;
  *    the caller owns all of them.  The library never allocates device
- *    memory: scratch lives in the caller's workspace.
+ *    memory: scratch lives in the caller's workspace (moe_lora_align_noalloc
+ *    alone uses a fixed array of the library's own instead).
  *  - bf16 tensors are passed as moelora_bf16 (uint16_t bit patterns),
  *    row-major, the reduction axis contiguous, 16-byte aligned.
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -108,6 +109,33 @@ int moe_lora_align(const moelora_dims* d, const int32_t* topk_ids_dev,
                    int32_t* sorted_ids_dev, int32_t* blk_expert_dev,
                    int32_t* seg_off_dev, int32_t* num_post_pad_dev,
                    void* ws_dev, size_t ws_bytes, moelora_stream_t stream);
+
+/*
+ * moe_lora_align_noalloc -- moe_lora_align without a workspace argument.
+ *
+ * The paper has no counterpart: this exists for callers that cannot
+ * allocate device memory -- code running while a stream is captured into a
+ * CUDA graph (a cudaMalloc there breaks the capture), plug-ins handed
+ * tensors but no allocator, and servers that reserved all device memory for
+ * their own pool.  It computes exactly what moe_lora_align computes, with
+ * the same inputs and outputs, but keeps its scratch in a fixed 4 MiB array
+ * inside the library's device memory and allocates nothing.
+ *   - Every GPU that loads the library holds those 4 MiB until process exit.
+ *   - Sizes whose align scratch exceeds 4 MiB (about 256*(T*k/256+1)*E*(L+1)*4
+ *     + 8*T*k + 4*E*(L+1) bytes) return MOELORA_ERR_WORKSPACE.
+ *   - All calls share the one array: calls whose GPU work overlaps (on
+ *     different streams without ordering) race; order them on one stream.
+ *   - The first call on each device looks up the array's device address;
+ *     make it before any stream capture.
+ *   - Out-of-range ids are left out of the order as in moe_lora_align, but
+ *     the device error flag is not readable (there is no workspace to pass to
+ *     moelora_get_error).
+ */
+int moe_lora_align_noalloc(const moelora_dims* d, const int32_t* topk_ids_dev,
+                           const int32_t* lora_ids_dev, int32_t block_m,
+                           int32_t* sorted_ids_dev, int32_t* blk_expert_dev,
+                           int32_t* seg_off_dev, int32_t* num_post_pad_dev,
+                           moelora_stream_t stream);
 
 /*
  * moe_lora_forward -- the fused MoE-LoRA expert layer (formula at the top).

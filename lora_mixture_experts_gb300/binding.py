@@ -50,6 +50,8 @@ _SIGS = {
     "moelora_align_capacity": (_SZ, [ctypes.POINTER(moelora_dims), _I32]),
     "moe_lora_align": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _I32, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
+    "moe_lora_align_noalloc": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _I32, _P, _P,
+                                              _P, _P, _P]),
     "moe_lora_forward": (ctypes.c_int, [ctypes.POINTER(moelora_dims)] + [_P] * 12 + [_SZ, _P]),
     "moe_lora_linear": (ctypes.c_int, [ctypes.POINTER(moelora_linear_dims)] + [_P] * 7 + [_SZ, _P]),
     "moelora_set_timing_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _I32]),
@@ -152,6 +154,26 @@ def moe_lora_align(topk_ids, lora_ids, E: int, L: int, block_m: int, ws=None, st
                             _ptr(sorted_ids), _ptr(blk), _ptr(seg), _ptr(npp), _ptr(ws),
                             ws.numel(), _stream(stream))
     _check(st, "moe_lora_align")
+    return sorted_ids[:cap], blk[:cap // block_m], seg, npp
+
+
+def moe_lora_align_noalloc(topk_ids, lora_ids, E: int, L: int, block_m: int, stream=None):
+    """moe_lora_align for callers that cannot allocate device scratch: the
+    library uses its own fixed 4 MiB device array instead of a workspace.
+    Returns (sorted_ids, blk_expert, seg_off, num_post_pad); the output
+    tensors are allocated here by torch only for the caller's convenience."""
+    lib = load()
+    T, k = topk_ids.shape
+    d = moelora_dims(T, k, E, 8, 8, L, 0)
+    cap = lib.moelora_align_capacity(ctypes.byref(d), block_m)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    blk = torch.empty(max(cap // max(block_m, 1), 1), dtype=torch.int32, device=dev)
+    seg = torch.empty(E * (L + 1) + 1, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    st = lib.moe_lora_align_noalloc(ctypes.byref(d), _ptr(topk_ids), _ptr(lora_ids), block_m,
+                                    _ptr(sorted_ids), _ptr(blk), _ptr(seg), _ptr(npp), _stream(stream))
+    _check(st, "moe_lora_align_noalloc")
     return sorted_ids[:cap], blk[:cap // block_m], seg, npp
 
 

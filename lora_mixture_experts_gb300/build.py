@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoelora.so")
-SOURCES = ["align_kernels.cu", "gemm_tc.cu", "moelora_api.cu"]
+SOURCES = ["align_kernels.cu", "gemm_tc.cu", "moelora_api.cu", "align_noalloc.cu"]
 HEADERS = ["common.cuh", "align.cuh", "gemm_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
