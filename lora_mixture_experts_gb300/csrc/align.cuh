@@ -58,8 +58,10 @@ cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool c
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
                            int Pmax, int H, int num_sms, cudaStream_t stream);
 
-// out[t] = sum_j y_pair[pos_of[t*k+j]] in fp32, j ascending, one bf16 rounding.
+// out[t] = sum_j sum_s y_pair[s][pos_of[t*k+j]] in fp32 (j ascending, then
+// the K splits s in order), one bf16 rounding.  split_stride in floats.
 cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
-                           int T, int k, int H, int num_sms, cudaStream_t stream);
+                           int T, int k, int H, int nsplit, long long split_stride,
+                           int num_sms, cudaStream_t stream);
 
 }  // namespace moelora

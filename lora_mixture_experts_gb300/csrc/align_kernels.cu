@@ -253,8 +253,9 @@ __global__ void permute_kernel(const uint4* __restrict__ x, const int* __restric
 }
 
 __global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __restrict__ pos_of,
-                               uint2* __restrict__ out, int T, int k, int hv) {
-  // hv = H / 4: four features per thread
+                               uint2* __restrict__ out, int T, int k, int hv, int nsplit,
+                               long long split_stride4) {
+  // hv = H / 4: four features per thread; partials summed j-major, split-minor
   grid_dependency_wait();
   grid_dependency_trigger();
   const size_t total = static_cast<size_t>(T) * hv;
@@ -266,11 +267,13 @@ __global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __r
     for (int j = 0; j < k; ++j) {
       const int pos = pos_of[t * k + j];
       if (pos < 0) continue;
-      const float4 v = y_pair[static_cast<size_t>(pos) * hv + c];
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      for (int s = 0; s < nsplit; ++s) {
+        const float4 v = y_pair[s * split_stride4 + static_cast<size_t>(pos) * hv + c];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
     }
     uint2 o;
     __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
@@ -310,14 +313,15 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bflo
 }
 
 cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
-                           int T, int k, int H, int num_sms, cudaStream_t stream) {
+                           int T, int k, int H, int nsplit, long long split_stride,
+                           int num_sms, cudaStream_t stream) {
   const int hv = H / 4;
   const size_t total = static_cast<size_t>(T) * hv;
   int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
   if (grid < 1) grid = 1;
   return launch_chained(combine_kernel, dim3(grid), dim3(256), 0, stream, true,
                         reinterpret_cast<const float4*>(y_pair), pos_of, reinterpret_cast<uint2*>(out),
-                        T, k, hv);
+                        T, k, hv, nsplit, split_stride / 4);
 }
 
 }  // namespace moelora

@@ -53,6 +53,7 @@ struct Item {
   int tile;
   int m;        // weight tile (main items)
   int sh;       // shrink item index
+  int ks;       // K split (main items)
 };
 
 // Item order: all shrink items first, then the main items in groups of
@@ -61,6 +62,12 @@ struct Item {
 // in the tile table) share each weight tile through L2 while it is hot, and
 // the group's token rows (sized by the host to a fraction of L2) stay
 // resident across all m.
+// Item order: all shrink items first, then the main items, K split by K
+// split; inside a split, groups of `gt` consecutive token tiles.  Inside a
+// group the weight tile m is the slow index and the tile the fast one, so the
+// tiles of one expert (adjacent in the tile table) share each weight tile
+// through L2 while it is hot, and the group's token rows (sized by the host
+// to a fraction of L2) stay resident across all m.
 __device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_m, int gt,
                                             const ShrinkItem* sh) {
   Item it;
@@ -69,8 +76,12 @@ __device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_
     it.sh = w;
     it.tile = sh[w].tile;
     it.m = 0;
+    it.ks = 0;
   } else {
     w -= n_sh;
+    const int per_split = n_tiles * n_m;
+    it.ks = w / per_split;
+    w -= it.ks * per_split;
     const int per_group = gt * n_m;
     const int g = w / per_group;
     const int wl = w - g * per_group;
@@ -156,8 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tiles = p.hdr->n_tiles;
   const int n_sh = p.r > 0 ? p.hdr->n_shrink : 0;
-  const int n_items = n_sh + n_tiles * p.n_mtiles;
-  const int nk = (p.K + 63) / 64;
+  const int n_items = n_sh + n_tiles * p.n_mtiles * p.ksplit;
+  const int nk = (p.K + 63) / 64;             // 64-wide K chunks of the base GEMM
+  const int nks = (nk + p.ksplit - 1) / p.ksplit;   // chunks per K split
   const bool gate_up = p.mode == kModeGateUp;
 
   if (warp == 0) {
@@ -189,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           const uint32_t bytes = kATileBytes + brows * 128;
-          for (int kc = 0; kc < nk && ok; ++kc, ++cnt) {
+          const int kc1 = min(nk, (it.ks + 1) * nks);
+          for (int kc = it.ks * nks; kc < kc1 && ok; ++kc, ++cnt) {
             const int s = cnt % C::kStages;
             const uint32_t ph = (cnt / C::kStages) & 1;
             if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
@@ -204,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tma_load_2d(a_s + kATileBytes, tb, fb, kc * 64, ti.row0);
           }
-          if (ok && p.r > 0 && ti.nslots > 0) {
+          if (ok && p.r > 0 && ti.nslots > 0 && it.ks == p.ksplit - 1) {
             // the tile's shrink results must be complete and visible to TMA
             const int target = p.done_target * ti.nsh;
             const uint64_t t0 = globaltimer_ns();
@@ -269,8 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(smem_u32(&acce_bar[buf]), ((li >> 1) & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * TN;
-        const int n_lora = (!it.shrink && p.r > 0) ? ti.nslots * p.lora_chunks : 0;
-        const int nch = nk + n_lora;
+        const int n_lora =
+            (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks : 0;
+        const int n_base = it.shrink ? nk : min(nk, (it.ks + 1) * nks) - it.ks * nks;
+        const int nch = n_base + n_lora;
         for (int ch = 0; ch < nch; ++ch, ++cnt) {
           const int s = cnt % C::kStages;
           const uint32_t ph = (cnt / C::kStages) & 1;
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
           const uint32_t b_s = a_s + kATileBytes;
-          const bool base = ch < nk;
+          const bool base = ch < n_base;
           const int width = base ? 64 : p.lora_w;
           const uint32_t swz = base ? 2u : static_cast<uint32_t>(p.lora_swz);
           const uint32_t sbo = base ? 1024u : static_cast<uint32_t>(8 * p.lora_w * 2);
@@ -390,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   p.out[static_cast<size_t>(p.row_tok[prow]) * p.out_ld + feat] =
                       __float2bfloat16_rn(v[cc]);
                 } else {
-                  p.out_f32[static_cast<size_t>(prow) * p.out_ld + feat] = v[cc] * p.row_w[prow];
+                  p.out_f32[it.ks * p.split_stride + static_cast<size_t>(prow) * p.out_ld + feat] =
+                      v[cc] * p.row_w[prow];
                 }
               }
             }

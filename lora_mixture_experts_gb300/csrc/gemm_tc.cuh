@@ -30,6 +30,8 @@ struct GemmParams {
   int slots_per_item;  // 128 / r
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
   int group_tiles;     // token tiles per L2 group of the main-item order
+  int ksplit;          // K splits of the main items (down mode: fp32 partial per split)
+  long long split_stride;  // elements between the fp32 partials of consecutive splits
   const WsHeader* hdr;
   int* err;
   const TileInfo* tiles;

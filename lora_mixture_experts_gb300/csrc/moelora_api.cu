@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -29,6 +30,7 @@ struct Plan {
   bool lora = false;
   int n = 0, nbins = 0, nchunks = 0, block_m = kBlockM, Pmax = 0, tn = 32;
   int n_tiles_max = 0, n_slots_max = 0, n_sh_max = 0;
+  int ksplit = 1;                     // K splits of the down / linear phase
   size_t off_hdr = 0, off_chunk_hist = 0, off_bin_of = 0, off_rank_of = 0, off_bin_start = 0;
   size_t off_sorted = 0, off_blk = 0, off_seg = 0;
   size_t off_row_tok = 0, off_row_lora = 0, off_row_w = 0, off_pos_of = 0;
@@ -109,6 +111,31 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   p.off_zgu = b.take(std::max<size_t>(zbytes, 16));
 }
 
+// K splits for the last GEMM phase.  Decode-sized batches have few token
+// tiles, so 128-row weight tiles alone give too few work items to fill the
+// SMs in whole waves; splitting K (partials summed in order by the combine)
+// multiplies the items.  Chosen from the sizes alone (workspace sizing must
+// not depend on the device), for the 152 SMs of a GB300.
+constexpr int kNominalSms = 152;
+
+int choose_ksplit(double est_tiles, int n_mtiles, int K, double rows_per_expert) {
+  if (rows_per_expert > 64) return 1;            // tensor-bound: no split
+  const int nk = (K + 63) / 64;
+  const double items = std::max(1.0, est_tiles) * n_mtiles;
+  // aim at >= 8 items per SM (short tail), keep >= 16 K-chunks per split
+  int s = static_cast<int>(std::ceil(8.0 * kNominalSms / items));
+  s = std::max(1, std::min(s, 4));
+  while (s > 1 && nk / s < 16) --s;
+  return s;
+}
+
+// Expected token tiles of a call: experts touched under uniform routing
+// plus the extra tiles of experts with more than tn rows.
+double expected_tiles(int T, int k, int E, int tn) {
+  const double touched = E * (1.0 - std::pow(1.0 - static_cast<double>(k) / E, T));
+  return std::floor(touched + 0.5) + std::floor(static_cast<double>(T) * k / tn);
+}
+
 Plan plan_forward(const moelora_dims* d) {
   Plan p;
   p.T = d->T; p.k = d->k; p.E = d->E; p.H = d->H; p.I = d->I;
@@ -121,7 +148,9 @@ Plan plan_forward(const moelora_dims* d) {
   const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
   p.off_zd = b.take(std::max<size_t>(zbytes, 16));
   p.off_act = b.take(static_cast<size_t>(p.Pmax) * p.I * 2);
-  p.off_ypair = b.take(static_cast<size_t>(p.Pmax) * p.H * 4);
+  p.ksplit = choose_ksplit(expected_tiles(p.T, p.k, p.E, p.tn), (p.H + 127) / 128, p.I,
+                           static_cast<double>(p.n) / p.E);
+  p.off_ypair = b.take(static_cast<size_t>(p.ksplit) * p.Pmax * p.H * 4);
   p.total = b.cur;
   return p;
 }
@@ -136,6 +165,10 @@ Plan plan_linear(const moelora_linear_dims* d) {
   Bump b;
   plan_align_scratch(p, b);
   plan_gemm_tables(p, b);
+  p.ksplit = choose_ksplit(std::ceil(static_cast<double>(p.T) / p.tn), (p.N + 127) / 128, p.H,
+                           static_cast<double>(p.T));
+  if (p.ksplit > 1)   // split partials in fp32, summed into out by the combine
+    p.off_ypair = b.take(static_cast<size_t>(p.ksplit) * p.Pmax * p.N * 4);
   p.total = b.cur;
   return p;
 }
@@ -343,6 +376,8 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
 GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
+  g.ksplit = 1;
+  g.split_stride = 0;
   g.r = p.r;
   g.lora_w = p.lora ? std::min(p.r, 64) : 64;
   g.lora_chunks = p.lora ? p.r / g.lora_w : 0;
@@ -512,6 +547,8 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   gd.zbuf = zd;
   gd.out = nullptr;
   gd.out_f32 = ypair;
+  gd.ksplit = p.ksplit;
+  gd.split_stride = static_cast<long long>(p.Pmax) * p.H;
   gd.out_ld = p.H;
 
   Launcher ln(stream);
@@ -523,10 +560,11 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   ln.before("gemm_gate_up");
   MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles, sms), stream));
   ln.before("gemm_down");
-  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles, sms), stream));
+  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles * p.ksplit, sms), stream));
   ln.before("combine");
   MOELORA_CUDA_CHECK(launch_combine(ypair, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
-                                    p.k, p.H, sms, stream));
+                                    p.k, p.H, p.ksplit, static_cast<long long>(p.Pmax) * p.H, sms,
+                                    stream));
   ln.finish();
   return MOELORA_OK;
 }
@@ -573,15 +611,24 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   if (!ok) return MOELORA_ERR_CUDA;
 
   GemmParams g = gemm_params(p, ws, a);
-  g.mode = kModeLinear;
   g.K = p.H;
   g.n_mtiles = (p.N + 127) / 128;
   g.out_feats = p.N;
   g.done_target = 1;
   g.group_tiles = group_tiles(p.tn, p.H);
   g.zbuf = z;
-  g.out = reinterpret_cast<__nv_bfloat16*>(out);
   g.out_ld = p.N;
+  g.ksplit = p.ksplit;
+  float* partial = p.ksplit > 1 ? ws_ptr<float>(ws, p.off_ypair) : nullptr;
+  if (p.ksplit > 1) {
+    // fp32 partial per K split (gate weight 1), summed by the combine
+    g.mode = kModeDown;
+    g.out_f32 = partial;
+    g.split_stride = static_cast<long long>(p.Pmax) * p.N;
+  } else {
+    g.mode = kModeLinear;
+    g.out = reinterpret_cast<__nv_bfloat16*>(out);
+  }
 
   Launcher ln(stream);
   MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
@@ -590,7 +637,13 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
                                     p.Pmax, p.H, sms, stream));
   ln.before("gemm_linear");
-  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, m, g, gemm_grid(p, g.n_mtiles, sms), stream));
+  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, m, g, gemm_grid(p, g.n_mtiles * p.ksplit, sms), stream));
+  if (p.ksplit > 1) {
+    ln.before("combine");
+    MOELORA_CUDA_CHECK(launch_combine(partial, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
+                                      1, p.N, p.ksplit, static_cast<long long>(p.Pmax) * p.N, sms,
+                                      stream));
+  }
   ln.finish();
   return MOELORA_OK;
 }

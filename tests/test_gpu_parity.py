@@ -130,6 +130,7 @@ SMALL = [
     (19, 192, 320, 5, 3, 2, 128),
     (40, 200, 136, 7, 2, 0, 0),      # no LoRA
     (300, 264, 264, 8, 2, 4, 16),    # several tiles per expert, ragged tail
+    (8, 136, 2048, 4, 2, 2, 16),     # few rows per expert, long K: the down phase splits K
 ]
 
 
