@@ -20,7 +20,11 @@
 // a few tokens streams weights at full width and a prefill tile uses N=256.
 // Operands arrive by TMA (128-byte swizzle, K-major) into a ring of shared
 // memory stages; one thread issues tcgen05.mma into a double-buffered TMEM
-// accumulator; four epilogue warps drain TMEM with tcgen05.ld.
+// accumulator; four epilogue warps drain TMEM with tcgen05.ld.  A stage holds
+// KB consecutive 64-wide K blocks (KB = 4 for 16-row token tiles, 2 for 32
+// and 64, 1 above): at decode sizes, where the weights stream from HBM, big
+// stages (64 KB of weights per barrier round trip) read markedly faster than
+// 16 KB ones.  The LoRA expand chunks of up to KB adapters share a stage.
 //
 // Shrink items precede main items in the item order and a main item's
 // producer waits (bounded) for its tile's shrink items before loading the
@@ -37,15 +41,18 @@ constexpr int kXchgStride = 17;          // floats per row of the gate/up exchan
 
 template <int TN>
 struct Cfg {
-  static constexpr int kStages = TN >= 256 ? 4 : 10;
-  static constexpr int kBTileBytes = TN * 128;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kNumBoxes = TN >= 256 ? 5 : (TN >= 128 ? 4 : (TN >= 64 ? 3 : (TN >= 32 ? 2 : 1)));
+  static constexpr int kKB = TN <= 16 ? 4 : (TN <= 64 ? 2 : 1);   // K blocks per stage
+  static constexpr int kBTileBytes = TN * 128;                      // per K block
+  static constexpr int kStageBytes = kKB * (kATileBytes + kBTileBytes);
+  static constexpr int kStages = TN <= 16 ? 3 : (TN <= 32 ? 5 : (TN <= 64 ? 4 : (TN <= 128 ? 6 : 4)));
   static constexpr int kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;
   static constexpr int kXchgBytes = 64 * kXchgStride * 4;
   static constexpr int kBarOff = kStages * kStageBytes + kXchgBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  // shared-memory offset of K block j's A / B tile inside a stage
+  __host__ __device__ static constexpr int a_off(int j) { return j * kATileBytes; }
+  __host__ __device__ static constexpr int b_off(int j) { return kKB * kATileBytes + j * kBTileBytes; }
 };
 
 struct Item {
@@ -56,12 +63,6 @@ struct Item {
   int ks;       // K split (main items)
 };
 
-// Item order: all shrink items first, then the main items in groups of
-// `gt` consecutive token tiles.  Inside a group the weight tile m is the
-// slow index and the tile the fast one, so the tiles of one expert (adjacent
-// in the tile table) share each weight tile through L2 while it is hot, and
-// the group's token rows (sized by the host to a fraction of L2) stay
-// resident across all m.
 // Item order: all shrink items first, then the main items, K split by K
 // split; inside a split, groups of `gt` consecutive token tiles.  Inside a
 // group the weight tile m is the slow index and the tile the fast one, so the
@@ -93,6 +94,18 @@ __device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_
     it.tile = t0 + (wl - it.m * ntg);
   }
   return it;
+}
+
+// First K chunk of a main item's loop.  Concurrent items start at different
+// K offsets so that their weight rows (all at the same column otherwise)
+// spread over the DRAM channels instead of camping on the few that one
+// column offset maps to when the row stride is a large power of two.  A pure
+// function of the item: the summation order, and so the result, is the same
+// on every run.
+__device__ __forceinline__ int k_rotation(const Item& it, int nkc) {
+  const unsigned h = static_cast<unsigned>(it.m) * 2654435761u + static_cast<unsigned>(it.tile) * 40503u +
+                     static_cast<unsigned>(it.ks) * 97u;
+  return static_cast<int>((h >> 7) % static_cast<unsigned>(nkc));
 }
 
 // Smallest box index i with (16 << i) >= n.
@@ -186,36 +199,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* tb = &maps.b[bi];
         if (it.shrink) {
           const ShrinkItem si = p.shrink[it.sh];
-          const uint32_t bytes = si.nslot * p.r * 128 + brows * 128;
-          for (int kc = 0; kc < nk && ok; ++kc, ++cnt) {
+          const uint32_t per_kb = si.nslot * p.r * 128 + brows * 128;
+          for (int kb0 = 0; kb0 < nk && ok; kb0 += C::kKB, ++cnt) {
+            const int nkb = min(C::kKB, nk - kb0);
             const int s = cnt % C::kStages;
             const uint32_t ph = (cnt / C::kStages) & 1;
             if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
             const uint32_t fb = smem_u32(&full_bar[s]);
-            const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
-            mbar_arrive_expect_tx(fb, bytes);
-            for (int j = 0; j < si.nslot; ++j)
-              tma_load_4d(a_s + j * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
-                          p.slot_adapter[si.slot0 + j]);
-            tma_load_2d(a_s + kATileBytes, tb, fb, kc * 64, ti.row0);
+            const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+            mbar_arrive_expect_tx(fb, nkb * per_kb);
+            for (int j = 0; j < nkb; ++j) {
+              const int kc = kb0 + j;
+              for (int q = 0; q < si.nslot; ++q)
+                tma_load_4d(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
+                            p.slot_adapter[si.slot0 + q]);
+              tma_load_2d(st + C::b_off(j), tb, fb, kc * 64, ti.row0);
+            }
           }
         } else {
-          const uint32_t bytes = kATileBytes + brows * 128;
-          const int kc1 = min(nk, (it.ks + 1) * nks);
-          for (int kc = it.ks * nks; kc < kc1 && ok; ++kc, ++cnt) {
+          const uint32_t per_kb = kATileBytes + brows * 128;
+          const int kc0 = it.ks * nks;
+          const int nkc = min(nk, kc0 + nks) - kc0;
+          const int rot = k_rotation(it, nkc);
+          for (int i0 = 0; i0 < nkc && ok; i0 += C::kKB, ++cnt) {
+            const int nkb = min(C::kKB, nkc - i0);
             const int s = cnt % C::kStages;
             const uint32_t ph = (cnt / C::kStages) & 1;
             if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
             const uint32_t fb = smem_u32(&full_bar[s]);
-            const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
-            mbar_arrive_expect_tx(fb, bytes);
-            if (gate_up) {
-              tma_load_3d(a_s, &maps.w, fb, kc * 64, it.m * 64, ti.expert);
-              tma_load_3d(a_s + 64 * 128, &maps.w, fb, kc * 64, p.half_rows + it.m * 64, ti.expert);
-            } else {
-              tma_load_3d(a_s, &maps.w, fb, kc * 64, it.m * 128, ti.expert);
+            const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+            mbar_arrive_expect_tx(fb, nkb * per_kb);
+            for (int j = 0; j < nkb; ++j) {
+              const int i = i0 + j;
+              const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
+              if (gate_up)   // gate rows m*64.. and up rows I+m*64.. in one box
+                tma_load_4d(st + C::a_off(j), &maps.w, fb, kc * 64, it.m * 64, 0, ti.expert);
+              else
+                tma_load_3d(st + C::a_off(j), &maps.w, fb, kc * 64, it.m * 128, ti.expert);
+              tma_load_2d(st + C::b_off(j), tb, fb, kc * 64, ti.row0);
             }
-            tma_load_2d(a_s + kATileBytes, tb, fb, kc * 64, ti.row0);
           }
           if (ok && p.r > 0 && ti.nslots > 0 && it.ks == p.ksplit - 1) {
             // the tile's shrink results must be complete and visible to TMA
@@ -231,24 +253,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_global();
             const CUtensorMap* tz = &maps.z[bi];
             const int lw = p.lora_w;
-            const uint32_t bytes_l = 128 * lw * 2 + brows * lw * 2;
-            for (int sl = 0; sl < ti.nslots && ok; ++sl) {
-              const int a = p.slot_adapter[ti.slot_base + sl];
-              for (int c = 0; c < p.lora_chunks && ok; ++c, ++cnt) {
-                const int s = cnt % C::kStages;
-                const uint32_t ph = (cnt / C::kStages) & 1;
-                if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
-                const uint32_t fb = smem_u32(&full_bar[s]);
-                const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
-                mbar_arrive_expect_tx(fb, bytes_l);
-                if (gate_up) {
-                  tma_load_4d(a_s, &maps.lb, fb, c * lw, it.m * 64, ti.expert, a);
-                  tma_load_4d(a_s + 64 * lw * 2, &maps.lb, fb, c * lw, p.half_rows + it.m * 64,
-                              ti.expert, a);
-                } else {
-                  tma_load_4d(a_s, &maps.lb, fb, c * lw, it.m * 128, ti.expert, a);
-                }
-                tma_load_2d(a_s + kATileBytes, tz, fb, c * lw, (ti.slot_base + sl) * TN);
+            const int nl = ti.nslots * p.lora_chunks;   // expand chunks: (slot, chunk) pairs
+            const uint32_t per_sub = 128 * lw * 2 + brows * lw * 2;
+            for (int i0 = 0; i0 < nl && ok; i0 += C::kKB, ++cnt) {
+              const int nsub = min(C::kKB, nl - i0);
+              const int s = cnt % C::kStages;
+              const uint32_t ph = (cnt / C::kStages) & 1;
+              if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
+              const uint32_t fb = smem_u32(&full_bar[s]);
+              const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+              mbar_arrive_expect_tx(fb, nsub * per_sub);
+              for (int j = 0; j < nsub; ++j) {
+                const int sl = (i0 + j) / p.lora_chunks;
+                const int c = (i0 + j) - sl * p.lora_chunks;
+                const int a = p.slot_adapter[ti.slot_base + sl];
+                if (gate_up)
+                  tma_load_5d(st + C::a_off(j), &maps.lb, fb, c * lw, it.m * 64, 0, ti.expert, a);
+                else
+                  tma_load_4d(st + C::a_off(j), &maps.lb, fb, c * lw, it.m * 128, ti.expert, a);
+                tma_load_2d(st + C::b_off(j), tz, fb, c * lw, (ti.slot_base + sl) * TN);
               }
             }
           }
@@ -282,26 +305,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(smem_u32(&acce_bar[buf]), ((li >> 1) & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * TN;
-        const int n_lora =
+        const int nl =
             (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks : 0;
-        const int n_base = it.shrink ? nk : min(nk, (it.ks + 1) * nks) - it.ks * nks;
-        const int nch = n_base + n_lora;
-        for (int ch = 0; ch < nch; ++ch, ++cnt) {
+        const int nb = it.shrink ? nk : min(nk, (it.ks + 1) * nks) - it.ks * nks;
+        const int st_base = (nb + C::kKB - 1) / C::kKB;
+        const int st_all = st_base + (nl + C::kKB - 1) / C::kKB;
+        bool first = true;
+        for (int sti = 0; sti < st_all; ++sti, ++cnt) {
           const int s = cnt % C::kStages;
           const uint32_t ph = (cnt / C::kStages) & 1;
           if (!(ok = mbar_wait(smem_u32(&full_bar[s]), ph, abort_flag))) break;
           tc_fence_after();
-          const uint32_t a_s = smem_u32(smem + s * C::kStageBytes);
-          const uint32_t b_s = a_s + kATileBytes;
-          const bool base = ch < n_base;
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const bool base = sti < st_base;
+          const int nsub = base ? min(C::kKB, nb - sti * C::kKB)
+                                : min(C::kKB, nl - (sti - st_base) * C::kKB);
           const int width = base ? 64 : p.lora_w;
           const uint32_t swz = base ? 2u : static_cast<uint32_t>(p.lora_swz);
           const uint32_t sbo = base ? 1024u : static_cast<uint32_t>(8 * p.lora_w * 2);
-          for (int kk = 0; kk < width / 16; ++kk) {
-            const uint64_t ad = make_smem_desc(a_s + kk * 32, sbo, swz);
-            const uint64_t bd = make_smem_desc(b_s + kk * 32, sbo, swz);
-            mma_bf16(d_tmem, ad, bd, idesc, (ch > 0 || kk > 0) ? 1u : 0u);
-            issued = true;
+          for (int j = 0; j < nsub; ++j) {
+            for (int kk = 0; kk < width / 16; ++kk) {
+              const uint64_t ad = make_smem_desc(st + C::a_off(j) + kk * 32, sbo, swz);
+              const uint64_t bd = make_smem_desc(st + C::b_off(j) + kk * 32, sbo, swz);
+              mma_bf16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
+              first = false;
+              issued = true;
+            }
           }
           mma_commit(smem_u32(&empty_bar[s]));
         }
@@ -447,13 +476,19 @@ cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaS
 }  // namespace
 
 size_t moe_gemm_smem_bytes(int tn) {
-  return tn >= 256 ? Cfg<256>::kSmemBytes : Cfg<32>::kSmemBytes;
+  return tn >= 256 ? Cfg<256>::kSmemBytes
+                   : (tn >= 128 ? Cfg<128>::kSmemBytes
+                                : (tn >= 64 ? Cfg<64>::kSmemBytes
+                                            : (tn >= 32 ? Cfg<32>::kSmemBytes : Cfg<16>::kSmemBytes)));
 }
 
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream) {
   if (tn == 256) return launch_tn<256>(maps, p, grid, stream);
+  if (tn == 128) return launch_tn<128>(maps, p, grid, stream);
+  if (tn == 64) return launch_tn<64>(maps, p, grid, stream);
   if (tn == 32) return launch_tn<32>(maps, p, grid, stream);
+  if (tn == 16) return launch_tn<16>(maps, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

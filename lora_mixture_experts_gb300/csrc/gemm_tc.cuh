@@ -10,8 +10,8 @@ enum GemmMode : int { kModeGateUp = 0, kModeDown = 1, kModeLinear = 2 };
 
 // Tensor maps of one GEMM phase.  b[i] / z[i] load 16 << i rows.
 struct alignas(64) GemmMaps {
-  CUtensorMap w;      // base weights, 3D (K, rows, E)
-  CUtensorMap lb;     // LoRA expand weights B, 4D (r, rows, E, L)
+  CUtensorMap w;      // base weights, 3D (K, rows, E); gate_up: 4D (K, I, 2, E)
+  CUtensorMap lb;     // LoRA expand weights B, 4D (r, rows, E, L); gate_up: 5D (r, I, 2, E, L)
   CUtensorMap la;     // LoRA shrink weights A, 4D (K, r, E, L)
   CUtensorMap b[5];   // token operand (x_perm or act), 2D (K, rows)
   CUtensorMap z[5];   // shrink results, 2D (r, slots * tn)
@@ -48,7 +48,7 @@ struct GemmParams {
 };
 
 // Launches one GEMM phase (shrink items first, then the main items) as a
-// persistent kernel on `grid` CTAs.  tn is 32 or 256.
+// persistent kernel on `grid` CTAs.  tn is 16, 32, 64, 128 or 256.
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream);
 

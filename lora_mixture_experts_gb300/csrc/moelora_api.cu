@@ -90,8 +90,10 @@ void plan_align_scratch(Plan& p, Bump& b) {
 
 void plan_gemm_tables(Plan& p, Bump& b) {
   p.Pmax = p.n + p.E * (p.block_m - 1);
-  const int avg = p.n / p.E;
-  p.tn = avg > 32 ? 256 : 32;
+  // token tile: the smallest of 16/32/64/128/256 rows that holds an average
+  // expert's rows (smaller tiles leave room for more pipeline stages)
+  const int avg = (p.n + p.E - 1) / p.E;
+  p.tn = avg <= 16 ? 16 : (avg <= 32 ? 32 : (avg <= 64 ? 64 : (avg <= 128 ? 128 : 256)));
   p.n_tiles_max = p.n / p.tn + std::min(p.E, std::max(p.n, 1)) + 1;
   p.n_slots_max = p.lora ? std::min(p.n, p.E * p.L + p.n_tiles_max) : 0;
   p.n_sh_max = p.n_slots_max;
@@ -257,6 +259,24 @@ bool enc3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
   const uint64_t str[2] = {d0, d0 * d1};
   const uint32_t box[3] = {b0, b1, 1};
   return encode_map(m, base, 3, dims, str, box);
+}
+
+// gate_up weight [E][2I][K] seen as (K, I, 2, E): one box brings the gate
+// rows and the matching up rows of a 64-feature block.
+bool enc_gate_up(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint64_t E) {
+  const uint64_t dims[4] = {K, I, 2, E};
+  const uint64_t str[3] = {K, I * K, 2 * I * K};
+  const uint32_t box[4] = {64, 64, 2, 1};
+  return encode_map(m, base, 4, dims, str, box);
+}
+
+// gate_up LoRA expand weight [L][E][2I][r] seen as (r, I, 2, E, L).
+bool enc_gate_up_lora(CUtensorMap* m, const void* base, uint64_t r, uint64_t I, uint64_t E,
+                      uint64_t L, uint32_t box_w) {
+  const uint64_t dims[5] = {r, I, 2, E, L};
+  const uint64_t str[4] = {r, I * r, 2 * I * r, 2 * I * r * E};
+  const uint32_t box[5] = {box_w, 64, 2, 1, 1};
+  return encode_map(m, base, 5, dims, str, box);
 }
 
 bool enc4(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
@@ -505,10 +525,10 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   // gate_up phase maps
   GemmMaps mg;
   std::memset(&mg, 0, sizeof(mg));
-  bool ok = enc3(&mg.w, W_gate_up, p.H, 2ull * p.I, p.E, 64, 64);
+  bool ok = enc_gate_up(&mg.w, W_gate_up, p.H, p.I, p.E);
   ok = ok && enc_row_maps(mg.b, x_perm, p.H, p.Pmax, 64, p.tn);
   if (p.lora) {
-    ok = ok && enc4(&mg.lb, B_gu, p.r, 2ull * p.I, p.E, p.L, lw, 64);
+    ok = ok && enc_gate_up_lora(&mg.lb, B_gu, p.r, p.I, p.E, p.L, lw);
     ok = ok && enc4(&mg.la, A_gu, p.H, p.r, p.E, p.L, 64, p.r);
     ok = ok && enc_row_maps(mg.z, zgu, p.r, zrows, lw, p.tn);
   }
