@@ -136,26 +136,36 @@ def workload_name(c):
 
 
 def source_hash():
+    """Hash of the GEMM kernel's sources: a DRAM-traffic figure captured by
+    ncu is reported only while the kernel it measured is unchanged."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "lora_mixture_experts_gb300", "csrc")
-    for n in sorted(os.listdir(d)):
+    for n in ("gemm_tc.cu", "gemm_tc.cuh", "common.cuh"):
         with open(os.path.join(d, n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(config_name, kernel):
-    """DRAM bytes per launch of `kernel` from a committed ncu capture, if the
-    kernel sources have not changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    if not os.path.exists(path):
+    """DRAM bytes per launch of `kernel` from the committed ncu summaries
+    (lines `traffic: config=... kernel=... bytes_per_launch=... source_hash=...`
+    in profiles/*.md), or None if none matches the current kernel source."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
         return None
-    with open(path) as f:
-        d = json.load(f)
-    e = d.get(config_name, {}).get(kernel)
-    if not e or e.get("source_hash") != source_hash():
-        return None
-    return e.get("bytes_per_launch")
+    want = source_hash()
+    for n in sorted(os.listdir(d)):
+        if not n.endswith(".md"):
+            continue
+        with open(os.path.join(d, n)) as f:
+            for line in f:
+                if not line.startswith("traffic:"):
+                    continue
+                kv = dict(tok.split("=", 1) for tok in line.split()[1:] if "=" in tok)
+                if (kv.get("config") == config_name and kv.get("kernel") == kernel
+                        and kv.get("source_hash") == want):
+                    return int(kv["bytes_per_launch"])
+    return None
 
 
 def cpu_cores():

@@ -54,6 +54,11 @@ cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream, bool chai
 cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream, bool chained);
 cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained);
 
+// The same align in one single-CTA kernel, for small batches.
+constexpr int kSmallMaxBins = 8192;
+bool align_small_fits(const AlignArgs& a);
+cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained);
+
 // x_perm[p] = x[row_tok[p]] (zero rows for padding), p < Pmax.
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
                            int Pmax, int H, int num_sms, cudaStream_t stream);

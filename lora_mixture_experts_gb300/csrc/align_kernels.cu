@@ -80,32 +80,21 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return excl;
 }
 
-__global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
-  __shared__ int warp_sums[32];
-  grid_dependency_wait();
-  grid_dependency_trigger();
+// Everything after the per-bin totals: expert counts and padding, segment
+// offsets, padding rows, block experts, and the GEMM tables.  `sb` is a
+// shared-memory array holding the per-bin entry counts; it is turned into
+// bin starts there (and copied to a.bin_start).  Reading the bins from shared
+// memory keeps the per-expert loops free of global round trips.  Run by all
+// kScanThreads threads of one CTA.
+__device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
   const int tid = threadIdx.x;
   const int Lp = a.L + 1;
-
-  // per-bin chunk offsets (in place) and totals (into bin_start)
-  for (int b = tid; b < a.nbins; b += kScanThreads) {
-    int run = 0;
-    for (int c = 0; c < a.nchunks; ++c) {
-      int* h = a.chunk_hist + static_cast<size_t>(c) * a.nbins + b;
-      const int v = *h;
-      *h = run;
-      run += v;
-    }
-    a.bin_start[b] = run;
-  }
-  __syncthreads();
-
   // one expert per thread
   const int e = tid;
   const bool has_e = e < a.E;
   int cnt = 0;
   if (has_e)
-    for (int l = 0; l < Lp; ++l) cnt += a.bin_start[e * Lp + l];
+    for (int l = 0; l < Lp; ++l) cnt += sb[e * Lp + l];
   const int pad = has_e ? (cnt + a.block_m - 1) / a.block_m * a.block_m : 0;
   int P;
   const int start = block_exclusive_scan(pad, warp_sums, &P);
@@ -115,7 +104,8 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
     int s = start;
     for (int l = 0; l < Lp; ++l) {
       const int b = e * Lp + l;
-      const int tot = a.bin_start[b];
+      const int tot = sb[b];
+      sb[b] = s;
       a.bin_start[b] = s;
       if (a.seg_off) a.seg_off[b] = s;
       s += tot;
@@ -159,8 +149,8 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
         const int s1 = min(start + cnt, s0 + a.tn);
         int ns = 0;
         for (int l = 1; l < Lp; ++l) {
-          const int lo = a.bin_start[e * Lp + l];
-          const int hi = (l + 1 < Lp) ? a.bin_start[e * Lp + l + 1] : start + cnt;
+          const int lo = sb[e * Lp + l];
+          const int hi = (l + 1 < Lp) ? sb[e * Lp + l + 1] : start + cnt;
           if (lo < hi && lo < s1 && hi > s0) ++ns;
         }
         n_s += ns;
@@ -187,8 +177,8 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
       int ns = 0;
       if (a.spi > 0) {
         for (int l = 1; l < Lp; ++l) {
-          const int lo = a.bin_start[e * Lp + l];
-          const int hi = (l + 1 < Lp) ? a.bin_start[e * Lp + l + 1] : start + cnt;
+          const int lo = sb[e * Lp + l];
+          const int hi = (l + 1 < Lp) ? sb[e * Lp + l + 1] : start + cnt;
           if (lo < hi && lo < s1 && hi > s0) a.slot_adapter[sl + ns++] = l - 1;
         }
       }
@@ -213,6 +203,81 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
     a.hdr->n_tiles = tot_t;
     a.hdr->n_slots = tot_s;
     a.hdr->n_shrink = tot_h;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
+  __shared__ int warp_sums[32];
+  extern __shared__ int sb[];   // [nbins]
+  grid_dependency_wait();
+  grid_dependency_trigger();
+  const int tid = threadIdx.x;
+
+  // per-bin chunk offsets (in place) and totals
+  for (int b = tid; b < a.nbins; b += kScanThreads) {
+    int run = 0;
+    for (int c = 0; c < a.nchunks; ++c) {
+      int* h = a.chunk_hist + static_cast<size_t>(c) * a.nbins + b;
+      const int v = *h;
+      *h = run;
+      run += v;
+    }
+    sb[b] = run;
+  }
+  __syncthreads();
+  align_tables(a, warp_sums, sb);
+}
+
+// The whole align in one CTA for up to kScanThreads entries (decode-sized
+// batches): bins, stable in-bin ranks (warps take turns in entry order, a
+// warp's lanes are ordered among themselves), totals, the shared tables
+// step, then the scatter.  Same results as hist + scan + scatter.
+__global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) {
+  __shared__ int warp_sums[32];
+  extern __shared__ int sm_bins[];   // [nbins] running counts
+  grid_dependency_wait();
+  grid_dependency_trigger();
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int f = tid;
+  int bin = -1;
+  if (f < a.n) {
+    const int e = a.topk_ids ? a.topk_ids[f] : 0;
+    const int l = a.lora_ignore ? -1 : a.lora_ids[f / a.k];
+    if (e < 0 || e >= a.E || l < -1 || l >= a.L)
+      flag_error(&a.hdr->err, kStatusBadIndex);
+    else
+      bin = e * (a.L + 1) + l + 1;
+  }
+  for (int b = tid; b < a.nbins; b += kScanThreads) sm_bins[b] = 0;
+  __syncthreads();
+  int rank = 0;
+  for (int w = 0; w < kScanThreads / 32; ++w) {
+    if (warp == w) {
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      const int leader = __ffs(peers) - 1;
+      if (bin >= 0) rank = sm_bins[bin] + __popc(peers & ((1u << lane) - 1));
+      __syncwarp();
+      if (bin >= 0 && lane == leader) sm_bins[bin] += __popc(peers);
+    }
+    __syncthreads();
+  }
+  align_tables(a, warp_sums, sm_bins);
+  __syncthreads();
+  if (f < a.n) {
+    if (bin < 0) {
+      if (a.pos_of) a.pos_of[f] = -1;
+    } else {
+      const int pos = sm_bins[bin] + rank;
+      a.sorted_ids[pos] = f;
+      if (a.row_tok) {
+        a.row_tok[pos] = f / a.k;
+        a.row_lora[pos] = bin % (a.L + 1) - 1;
+        a.row_w[pos] = a.topk_weights ? a.topk_weights[f] : 1.0f;
+        a.pos_of[f] = pos;
+      }
+    }
   }
 }
 
@@ -292,7 +357,17 @@ cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream, bool chai
 }
 
 cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream, bool chained) {
-  return launch_chained(align_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, chained, a);
+  return launch_chained(align_scan_kernel, dim3(1), dim3(kScanThreads), a.nbins * sizeof(int),
+                        stream, chained, a);
+}
+
+bool align_small_fits(const AlignArgs& a) {
+  return a.n <= kScanThreads && a.nbins <= kSmallMaxBins && a.E <= kScanThreads;
+}
+
+cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained) {
+  return launch_chained(align_small_kernel, dim3(1), dim3(kScanThreads), a.nbins * sizeof(int),
+                        stream, chained, a);
 }
 
 cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained) {

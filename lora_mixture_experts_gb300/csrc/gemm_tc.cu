@@ -190,9 +190,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t cnt = 0;
       bool ok = true;
+      // the next item's table entries are loaded one item ahead
+      Item it_next{};
+      TileInfo ti_next{};
+      if (static_cast<int>(blockIdx.x) < n_items) {
+        it_next = decode_item(blockIdx.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+        ti_next = p.tiles[it_next.tile];
+      }
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-        const TileInfo ti = p.tiles[it.tile];
+        const Item it = it_next;
+        const TileInfo ti = ti_next;
+        if (w + static_cast<int>(gridDim.x) < n_items) {
+          it_next = decode_item(w + gridDim.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+          ti_next = p.tiles[it_next.tile];
+        }
         const int nmma = (ti.nrows + 15) & ~15;
         const int bi = box_index(nmma);
         const int brows = 16 << bi;
@@ -296,9 +307,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t li = 0;
       bool ok = true;
       bool issued = false;
+      Item it_next{};
+      TileInfo ti_next{};
+      if (static_cast<int>(blockIdx.x) < n_items) {
+        it_next = decode_item(blockIdx.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+        ti_next = p.tiles[it_next.tile];
+      }
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++li) {
-        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-        const TileInfo ti = p.tiles[it.tile];
+        const Item it = it_next;
+        const TileInfo ti = ti_next;
+        if (w + static_cast<int>(gridDim.x) < n_items) {
+          it_next = decode_item(w + gridDim.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+          ti_next = p.tiles[it_next.tile];
+        }
         const int nmma = (ti.nrows + 15) & ~15;
         const uint32_t idesc = make_idesc_bf16(nmma);
         const int buf = li & 1;

@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -47,6 +48,16 @@ struct Bump {
     return at;
   }
 };
+
+// Tuning overrides for benchmarking: MOELORA_KSPLIT (1..4) and MOELORA_TN
+// (16, 32, 64, 128, 256).  Read at planning time, so the workspace size and
+// the call agree; unset means the built-in choice.
+int env_override(const char* name, int lo, int hi) {
+  const char* v = std::getenv(name);
+  if (!v) return 0;
+  const int x = std::atoi(v);
+  return (x >= lo && x <= hi) ? x : 0;
+}
 
 bool lora_rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
 
@@ -94,6 +105,8 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   // expert's rows (smaller tiles leave room for more pipeline stages)
   const int avg = (p.n + p.E - 1) / p.E;
   p.tn = avg <= 16 ? 16 : (avg <= 32 ? 32 : (avg <= 64 ? 64 : (avg <= 128 ? 128 : 256)));
+  if (const int f = env_override("MOELORA_TN", 16, 256))
+    if (f == 16 || f == 32 || f == 64 || f == 128 || f == 256) p.tn = f;
   p.n_tiles_max = p.n / p.tn + std::min(p.E, std::max(p.n, 1)) + 1;
   p.n_slots_max = p.lora ? std::min(p.n, p.E * p.L + p.n_tiles_max) : 0;
   p.n_sh_max = p.n_slots_max;
@@ -121,14 +134,16 @@ void plan_gemm_tables(Plan& p, Bump& b) {
 constexpr int kNominalSms = 152;
 
 int choose_ksplit(double est_tiles, int n_mtiles, int K, double rows_per_expert) {
+  if (const int f = env_override("MOELORA_KSPLIT", 1, 4)) return f;
   if (rows_per_expert > 64) return 1;            // tensor-bound: no split
   const int nk = (K + 63) / 64;
+  if (nk / 2 < 16) return 1;                     // keep >= 16 K blocks per split
   const double items = std::max(1.0, est_tiles) * n_mtiles;
-  // aim at >= 8 items per SM (short tail), keep >= 16 K-chunks per split
-  int s = static_cast<int>(std::ceil(8.0 * kNominalSms / items));
-  s = std::max(1, std::min(s, 4));
-  while (s > 1 && nk / s < 16) --s;
-  return s;
+  if (items >= 8.0 * kNominalSms) return 1;      // enough items for a short tail
+  auto eff = [](double n) { return n / (std::ceil(n / kNominalSms) * kNominalSms); };
+  // two splits when that does not worsen the last wave (measured: more than
+  // two splits costs more in partial traffic than it gains in balance)
+  return eff(2 * items) >= eff(items) ? 2 : 1;
 }
 
 // Expected token tiles of a call: experts touched under uniform routing
@@ -331,9 +346,14 @@ struct Launcher {
   }
 };
 
-// The align kernels; the first one follows a memset and is not chained.
+// The align kernels (one kernel for small batches); the first follows a
+// memset and is not chained.
 cudaError_t run_align(Launcher& ln, const AlignArgs& a, cudaStream_t stream) {
   cudaError_t e;
+  if (a.n > 0 && align_small_fits(a)) {
+    ln.before("align_small");
+    return launch_align_small(a, stream, false);
+  }
   bool first = true;
   if (a.nchunks > 0) {
     ln.before("align_hist");
