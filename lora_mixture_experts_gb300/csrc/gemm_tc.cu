@@ -26,30 +26,43 @@
 // stages (64 KB of weights per barrier round trip) read markedly faster than
 // 16 KB ones.  The LoRA expand chunks of up to KB adapters share a stage.
 //
+// 256-token tiles run on CTA pairs (2-SM MMA): the two CTAs of a cluster
+// share every item, each loading its 128 weight rows and half of the token
+// rows; the even CTA issues tcgen05.mma.cta_group::2 (M = 256) whose D rows
+// land in both CTAs' TMEM, and both CTAs drain their own half.  Per SM this
+// halves the token-operand bytes of a K block and lets a stage carry two K
+// blocks (64 KB), which is what the tensor-bound prefill tiles need: TMA
+// streaming from L2 measured 9 TB/s with 16 KB stages but 19-25 TB/s with 64 KB.
+//
 // Shrink items precede main items in the item order and a main item's
 // producer waits (bounded) for its tile's shrink items before loading the
-// z chunks.  Every CTA of the persistent grid is resident at once (grid <=
-// SM count, one CTA per SM), so the wait always ends.
+// z chunks.  Every CTA (pair) of the persistent grid is resident at once
+// (grid <= what fits, one CTA per SM), so the wait always ends.
 #include "gemm_tc.cuh"
+
+#include <algorithm>
 
 namespace moelora {
 namespace {
 
 constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
-constexpr int kXchgStride = 17;          // floats per row of the gate/up exchange
+constexpr int kXchgStride = 17;          // floats per row of a gate/up exchange buffer
 
-template <int TN>
+template <int TN, bool PAIR>
 struct Cfg {
-  static constexpr int kKB = TN <= 16 ? 4 : (TN <= 64 ? 2 : 1);   // K blocks per stage
-  static constexpr int kBTileBytes = TN * 128;                      // per K block
+  static constexpr int kRowsB = PAIR ? TN / 2 : TN;   // token rows a CTA holds per K block
+  static constexpr int kKB = PAIR ? 2 : (TN <= 16 ? 4 : (TN <= 64 ? 2 : 1));   // K blocks per stage
+  static constexpr int kBTileBytes = kRowsB * 128;                  // per K block
   static constexpr int kStageBytes = kKB * (kATileBytes + kBTileBytes);
-  static constexpr int kStages = TN <= 16 ? 3 : (TN <= 32 ? 5 : (TN <= 64 ? 4 : (TN <= 128 ? 6 : 4)));
+  static constexpr int kStages =
+      PAIR ? 3 : (TN <= 16 ? 3 : (TN <= 32 ? 5 : (TN <= 64 ? 4 : (TN <= 128 ? 6 : 4))));
   static constexpr int kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;
-  static constexpr int kXchgBytes = 64 * kXchgStride * 4;
+  static constexpr int kXchgBytes = 2 * 64 * kXchgStride * 4;   // gate and up halves
   static constexpr int kBarOff = kStages * kStageBytes + kXchgBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  static constexpr int kMRows = PAIR ? 256 : 128;   // weight rows of one item
   // shared-memory offset of K block j's A / B tile inside a stage
   __host__ __device__ static constexpr int a_off(int j) { return j * kATileBytes; }
   __host__ __device__ static constexpr int b_off(int j) { return kKB * kATileBytes + j * kBTileBytes; }
@@ -128,10 +141,10 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-template <int TN>
+template <int TN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using C = Cfg<TN>;
+  using C = Cfg<TN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -147,6 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: rank 0 leads; items are shared by the two CTAs of a cluster
+  const uint32_t rank = PAIR ? cluster_rank() : 0;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int n_units = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -155,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&accf_bar[b]), 1);
-      mbar_init(smem_u32(&acce_bar[b]), 4);
+      mbar_init(smem_u32(&acce_bar[b]), PAIR ? 8 : 4);   // epilogue warps of both CTAs
     }
     mbar_init(smem_u32(drain_bar), 1);
     *abort_flag = 0;
@@ -168,13 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&maps.la);
     }
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+  if (warp == 1) {
+    if (PAIR)
+      tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
+    else
+      tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+  }
   // results of the preceding launch (x_perm / act, the tile tables) are read
   // only after this point; the next launch may start its own preamble
   grid_dependency_wait();
   grid_dependency_trigger();
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -184,6 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = (p.K + 63) / 64;             // 64-wide K chunks of the base GEMM
   const int nks = (nk + p.ksplit - 1) / p.ksplit;   // chunks per K split
   const bool gate_up = p.mode == kModeGateUp;
+  const int spc = p.r > 0 ? 128 / p.r : 0;    // shrink slots per CTA
+  // shrink completions a tile's item waits for: every CTA of the item signals
+  const int done_scale = PAIR ? 2 : 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -193,66 +220,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next item's table entries are loaded one item ahead
       Item it_next{};
       TileInfo ti_next{};
-      if (static_cast<int>(blockIdx.x) < n_items) {
-        it_next = decode_item(blockIdx.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+      if (unit < n_items) {
+        it_next = decode_item(unit, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
         ti_next = p.tiles[it_next.tile];
       }
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      // one TMA load into this CTA's shared memory, counted on the leader's
+      // full barrier when paired
+      auto load2 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y) {
+        if (PAIR) tma_load_2d_pair(dst, m, fb, x, y); else tma_load_2d(dst, m, fb, x, y);
+      };
+      auto load3 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z) {
+        if (PAIR) tma_load_3d_pair(dst, m, fb, x, y, z); else tma_load_3d(dst, m, fb, x, y, z);
+      };
+      auto load4 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z, int w) {
+        if (PAIR) tma_load_4d_pair(dst, m, fb, x, y, z, w); else tma_load_4d(dst, m, fb, x, y, z, w);
+      };
+      auto load5 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z, int w,
+                       int v) {
+        if (PAIR) tma_load_5d_pair(dst, m, fb, x, y, z, w, v); else tma_load_5d(dst, m, fb, x, y, z, w, v);
+      };
+      // stage s of this CTA is free: wait on its empty barrier; the barrier
+      // that counts the stage's bytes is the leader's full barrier
+      auto acquire = [&](int s, uint32_t ph, uint32_t& fb) -> bool {
+        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag)) return false;
+        fb = PAIR ? mapa_shared(smem_u32(&full_bar[s]), 0) : smem_u32(&full_bar[s]);
+        return true;
+      };
+      for (int w = unit; w < n_items && ok; w += n_units) {
         const Item it = it_next;
         const TileInfo ti = ti_next;
-        if (w + static_cast<int>(gridDim.x) < n_items) {
-          it_next = decode_item(w + gridDim.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+        if (w + n_units < n_items) {
+          it_next = decode_item(w + n_units, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
           ti_next = p.tiles[it_next.tile];
         }
         const int nmma = (ti.nrows + 15) & ~15;
-        const int bi = box_index(nmma);
+        const int nh = PAIR ? nmma / 2 : nmma;          // token rows this CTA loads
+        const int bi = box_index(nh);
         const int brows = 16 << bi;
         const CUtensorMap* tb = &maps.b[bi];
+        const int brow0 = ti.row0 + static_cast<int>(rank) * nh;
         if (it.shrink) {
           const ShrinkItem si = p.shrink[it.sh];
-          const uint32_t per_kb = si.nslot * p.r * 128 + brows * 128;
+          // this CTA stacks slots [rank*spc, rank*spc + ns_me) of the item
+          const int ns0 = min(spc, si.nslot);
+          const int ns1 = PAIR ? max(0, si.nslot - spc) : 0;
+          const int ns_me = rank == 0 ? ns0 : ns1;
+          const uint32_t per_kb = (ns0 + ns1) * p.r * 128 + (PAIR ? 2 : 1) * brows * 128;
           for (int kb0 = 0; kb0 < nk && ok; kb0 += C::kKB, ++cnt) {
             const int nkb = min(C::kKB, nk - kb0);
             const int s = cnt % C::kStages;
-            const uint32_t ph = (cnt / C::kStages) & 1;
-            if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
-            const uint32_t fb = smem_u32(&full_bar[s]);
+            uint32_t fb;
+            if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-            mbar_arrive_expect_tx(fb, nkb * per_kb);
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
               const int kc = kb0 + j;
-              for (int q = 0; q < si.nslot; ++q)
-                tma_load_4d(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
-                            p.slot_adapter[si.slot0 + q]);
-              tma_load_2d(st + C::b_off(j), tb, fb, kc * 64, ti.row0);
+              for (int q = 0; q < ns_me; ++q)
+                load4(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
+                      p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
+              load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
           }
         } else {
-          const uint32_t per_kb = kATileBytes + brows * 128;
+          const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
           const int kc0 = it.ks * nks;
           const int nkc = min(nk, kc0 + nks) - kc0;
           const int rot = k_rotation(it, nkc);
+          // this CTA's 128 weight rows: gate_up features m*64*(1+PAIR) + rank*64,
+          // down / linear rows m*kMRows + rank*128
+          const int grow = gate_up ? it.m * (PAIR ? 128 : 64) + static_cast<int>(rank) * 64
+                                   : it.m * C::kMRows + static_cast<int>(rank) * 128;
           for (int i0 = 0; i0 < nkc && ok; i0 += C::kKB, ++cnt) {
             const int nkb = min(C::kKB, nkc - i0);
             const int s = cnt % C::kStages;
-            const uint32_t ph = (cnt / C::kStages) & 1;
-            if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
-            const uint32_t fb = smem_u32(&full_bar[s]);
+            uint32_t fb;
+            if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-            mbar_arrive_expect_tx(fb, nkb * per_kb);
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
               const int i = i0 + j;
               const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
-              if (gate_up)   // gate rows m*64.. and up rows I+m*64.. in one box
-                tma_load_4d(st + C::a_off(j), &maps.w, fb, kc * 64, it.m * 64, 0, ti.expert);
+              if (gate_up)   // gate rows and the matching up rows in one box
+                load4(st + C::a_off(j), &maps.w, fb, kc * 64, grow, 0, ti.expert);
               else
-                tma_load_3d(st + C::a_off(j), &maps.w, fb, kc * 64, it.m * 128, ti.expert);
-              tma_load_2d(st + C::b_off(j), tb, fb, kc * 64, ti.row0);
+                load3(st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
+              load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
           }
           if (ok && p.r > 0 && ti.nslots > 0 && it.ks == p.ksplit - 1) {
             // the tile's shrink results must be complete and visible to TMA
-            const int target = p.done_target * ti.nsh;
+            const int target = p.done_target * ti.nsh * done_scale;
             const uint64_t t0 = globaltimer_ns();
             while (ld_acquire_gpu(&p.tile_done[it.tile]) < target) {
               if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -265,24 +322,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* tz = &maps.z[bi];
             const int lw = p.lora_w;
             const int nl = ti.nslots * p.lora_chunks;   // expand chunks: (slot, chunk) pairs
-            const uint32_t per_sub = 128 * lw * 2 + brows * lw * 2;
+            const uint32_t per_sub = (PAIR ? 2 : 1) * (128 * lw * 2 + brows * lw * 2);
             for (int i0 = 0; i0 < nl && ok; i0 += C::kKB, ++cnt) {
               const int nsub = min(C::kKB, nl - i0);
               const int s = cnt % C::kStages;
-              const uint32_t ph = (cnt / C::kStages) & 1;
-              if (!(ok = mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))) break;
-              const uint32_t fb = smem_u32(&full_bar[s]);
+              uint32_t fb;
+              if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
               const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-              mbar_arrive_expect_tx(fb, nsub * per_sub);
+              if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nsub * per_sub);
               for (int j = 0; j < nsub; ++j) {
                 const int sl = (i0 + j) / p.lora_chunks;
                 const int c = (i0 + j) - sl * p.lora_chunks;
                 const int a = p.slot_adapter[ti.slot_base + sl];
                 if (gate_up)
-                  tma_load_5d(st + C::a_off(j), &maps.lb, fb, c * lw, it.m * 64, 0, ti.expert, a);
+                  load5(st + C::a_off(j), &maps.lb, fb, c * lw, grow, 0, ti.expert, a);
                 else
-                  tma_load_4d(st + C::a_off(j), &maps.lb, fb, c * lw, it.m * 128, ti.expert, a);
-                tma_load_2d(st + C::b_off(j), tz, fb, c * lw, (ti.slot_base + sl) * TN);
+                  load4(st + C::a_off(j), &maps.lb, fb, c * lw, grow, ti.expert, a);
+                load2(st + C::b_off(j), tz, fb, c * lw,
+                      (ti.slot_base + sl) * TN + static_cast<int>(rank) * nh);
               }
             }
           }
@@ -292,36 +349,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         flag_error(p.err, kStatusTimeout);
         // let the copies already issued land before the CTA exits
-        const uint32_t first = cnt > (uint32_t)C::kStages ? cnt - C::kStages : 0;
-        for (uint32_t c = first; c < cnt; ++c) {
+        if (PAIR) {
+          // (their completions count on the leader's barriers: give them time)
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(smem_u32(&full_bar[c % C::kStages]), (c / C::kStages) & 1))
-            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+          while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+        } else {
+          const uint32_t first = cnt > (uint32_t)C::kStages ? cnt - C::kStages : 0;
+          for (uint32_t c = first; c < cnt; ++c) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&full_bar[c % C::kStages]), (c / C::kStages) & 1))
+              if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t cnt = 0;
       uint32_t li = 0;
       bool ok = true;
       bool issued = false;
       Item it_next{};
       TileInfo ti_next{};
-      if (static_cast<int>(blockIdx.x) < n_items) {
-        it_next = decode_item(blockIdx.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+      if (unit < n_items) {
+        it_next = decode_item(unit, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
         ti_next = p.tiles[it_next.tile];
       }
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++li) {
+      for (int w = unit; w < n_items && ok; w += n_units, ++li) {
         const Item it = it_next;
         const TileInfo ti = ti_next;
-        if (w + static_cast<int>(gridDim.x) < n_items) {
-          it_next = decode_item(w + gridDim.x, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+        if (w + n_units < n_items) {
+          it_next = decode_item(w + n_units, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
           ti_next = p.tiles[it_next.tile];
         }
         const int nmma = (ti.nrows + 15) & ~15;
-        const uint32_t idesc = make_idesc_bf16(nmma);
+        const uint32_t idesc = make_idesc_bf16(nmma, PAIR ? 256 : 128);
         const int buf = li & 1;
         if (!(ok = mbar_wait(smem_u32(&acce_bar[buf]), ((li >> 1) & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
@@ -348,14 +411,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < width / 16; ++kk) {
               const uint64_t ad = make_smem_desc(st + C::a_off(j) + kk * 32, sbo, swz);
               const uint64_t bd = make_smem_desc(st + C::b_off(j) + kk * 32, sbo, swz);
-              mma_bf16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
+              if (PAIR)
+                mma_bf16_pair(d_tmem, ad, bd, idesc, first ? 0u : 1u);
+              else
+                mma_bf16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
               first = false;
               issued = true;
             }
           }
-          mma_commit(smem_u32(&empty_bar[s]));
+          if (PAIR) mma_commit_pair(smem_u32(&empty_bar[s])); else mma_commit(smem_u32(&empty_bar[s]));
         }
-        if (ok) mma_commit(smem_u32(&accf_bar[buf]));
+        if (ok) {
+          if (PAIR) mma_commit_pair(smem_u32(&accf_bar[buf])); else mma_commit(smem_u32(&accf_bar[buf]));
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -363,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok && issued) {
         // wait (bounded) for the MMAs in flight before TMEM is released
-        mma_commit(smem_u32(drain_bar));
+        if (PAIR) mma_commit_pair(smem_u32(drain_bar)); else mma_commit(smem_u32(drain_bar));
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(drain_bar), 0))
           if (globaltimer_ns() - t0 > kWaitLimitNs) break;
@@ -372,9 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;     // accumulator row = weight row of the tile
+    const int row = quarter * 32 + lane;     // accumulator row = weight row of this CTA's half
+    // the MMA issuer's "accumulator free" barrier (the leader's, when paired)
+    const uint32_t acce0 = PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : smem_u32(&acce_bar[0]);
     uint32_t li = 0;
-    for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++li) {
+    for (int w = unit; w < n_items; w += n_units, ++li) {
       const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
       const TileInfo ti = p.tiles[it.tile];
       const int nmma = (ti.nrows + 15) & ~15;
@@ -390,11 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (it.shrink) {
         const ShrinkItem si = p.shrink[it.sh];
-        const int j = row / p.r;
-        const int q = row - j * p.r;
-        const bool valid = j < si.nslot;
+        const int j = static_cast<int>(rank) * spc + row / p.r;   // slot of the item
+        const int q = row % p.r;
+        const bool valid = j < si.nslot && row / p.r < spc;
         const int a_j = valid ? p.slot_adapter[si.slot0 + j] : -3;
-        __nv_bfloat16* zrow = p.zbuf + (static_cast<size_t>(si.slot0 + j) * TN) * p.r + q;
+        __nv_bfloat16* zrow = p.zbuf + (static_cast<size_t>(si.slot0 + (valid ? j : 0)) * TN) * p.r + q;
         for (int c0 = 0; c0 < nmma; c0 += 16) {
           float v[16];
           tmem_ld16(t_row + c0, v);
@@ -415,32 +485,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicAdd(&p.tile_done[it.tile], 1);
         }
       } else if (gate_up) {
+        // TMEM lanes 0-63 hold the gate rows and 64-127 the up rows of the
+        // same 64 features.  Per chunk of W columns the gate warps finish the
+        // first W/2 columns and the up warps the last W/2, each after taking
+        // the other half's values from a small shared-memory exchange.
         const bool is_gate = row < 64;
         const int f = row & 63;
-        const int feat = it.m * 64 + f;
+        const int feat = it.m * (PAIR ? 128 : 64) + static_cast<int>(rank) * 64 + f;
+        float* xg = xchg;                          // gate values of the up warps' columns
+        float* xu = xchg + 64 * kXchgStride;       // up values of the gate warps' columns
         __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0) * p.out_ld + feat;
-        for (int c0 = 0; c0 < nmma; c0 += 16) {
+        const bool store_ok = feat < p.out_feats;
+        auto finish = [&](const float* v, int c0, int half) {
+          // v: this thread's W = 2*half values of columns c0 .. c0+W-1
+          if (is_gate) {
+            for (int cc = 0; cc < half; ++cc) xg[f * kXchgStride + cc] = v[half + cc];
+          } else {
+            for (int cc = 0; cc < half; ++cc) xu[f * kXchgStride + cc] = v[cc];
+          }
+          named_bar_sync(1, 128);
+          const int cbase = c0 + (is_gate ? 0 : half);
+          for (int cc = 0; cc < half; ++cc) {
+            const int c = cbase + cc;
+            const float g = is_gate ? v[cc] : xg[f * kXchgStride + cc];
+            const float u = is_gate ? xu[f * kXchgStride + cc] : v[half + cc];
+            if (store_ok && c < ti.nrows)
+              orow[static_cast<size_t>(c) * p.out_ld] = __float2bfloat16_rn(silu_f(g) * u);
+          }
+          named_bar_sync(1, 128);
+        };
+        int c0 = 0;
+        for (; c0 + 32 <= nmma; c0 += 32) {
+          float v[32];
+          tmem_ld32(t_row + c0, v);
+          finish(v, c0, 16);
+        }
+        if (c0 < nmma) {   // a last chunk of 16 columns
           float v[16];
           tmem_ld16(t_row + c0, v);
-          if (!is_gate) {
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) xchg[f * kXchgStride + cc] = v[cc];
-          }
-          named_bar_sync(1, 128);
-          if (is_gate && feat < p.out_feats) {
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) {
-              const int c = c0 + cc;
-              if (c < ti.nrows) {
-                const float u = xchg[f * kXchgStride + cc];
-                orow[static_cast<size_t>(c) * p.out_ld] = __float2bfloat16_rn(silu_f(v[cc]) * u);
-              }
-            }
-          }
-          named_bar_sync(1, 128);
+          finish(v, c0, 8);
         }
       } else {
-        const int feat = it.m * 128 + row;
+        const int feat = it.m * C::kMRows + static_cast<int>(rank) * 128 + row;
         const bool linear = p.mode == kModeLinear;
         for (int c0 = 0; c0 < nmma; c0 += 16) {
           float v[16];
@@ -465,51 +551,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce_bar[buf]));
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(acce0 + buf * 8);
+        else
+          mbar_arrive(acce0 + buf * 8);
+      }
     }
   }
 
   __syncthreads();
+  if (PAIR) cluster_sync();   // no CTA leaves while its peer may still touch it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-template <int TN>
+template <int TN, bool PAIR>
 cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
-  using C = Cfg<TN>;
+  using C = Cfg<TN, PAIR>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static int configured_device = -1;
+  static int max_units = 0;   // co-resident CTAs (pairs count as one unit)
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<TN>,
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<TN, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<TN, PAIR>, &cfg);
+      if (e != cudaSuccess) return e;
+      max_units = clusters;
+    } else {
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_gemm_kernel<TN, PAIR>, kThreads,
+                                                        C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      max_units = per_sm * sms;
+    }
+    if (max_units < 1) return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
-  return launch_chained(moe_gemm_kernel<TN>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream,
-                        true, maps, p);
+  // every CTA (pair) must be resident at once: items wait on one another
+  const int units = std::max(1, std::min(grid, max_units));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(PAIR ? 2 * units : units);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (PAIR) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    na = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<TN, PAIR>, maps, p);
 }
 
 }  // namespace
 
 size_t moe_gemm_smem_bytes(int tn) {
-  return tn >= 256 ? Cfg<256>::kSmemBytes
-                   : (tn >= 128 ? Cfg<128>::kSmemBytes
-                                : (tn >= 64 ? Cfg<64>::kSmemBytes
-                                            : (tn >= 32 ? Cfg<32>::kSmemBytes : Cfg<16>::kSmemBytes)));
+  return tn >= 256 ? Cfg<256, true>::kSmemBytes
+                   : (tn >= 128 ? Cfg<128, false>::kSmemBytes
+                                : (tn >= 64 ? Cfg<64, false>::kSmemBytes
+                                            : (tn >= 32 ? Cfg<32, false>::kSmemBytes
+                                                        : Cfg<16, false>::kSmemBytes)));
 }
+
+bool moe_gemm_paired(int tn) { return tn >= 256; }
 
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream) {
-  if (tn == 256) return launch_tn<256>(maps, p, grid, stream);
-  if (tn == 128) return launch_tn<128>(maps, p, grid, stream);
-  if (tn == 64) return launch_tn<64>(maps, p, grid, stream);
-  if (tn == 32) return launch_tn<32>(maps, p, grid, stream);
-  if (tn == 16) return launch_tn<16>(maps, p, grid, stream);
+  if (tn == 256) return launch_tn<256, true>(maps, p, grid, stream);
+  if (tn == 128) return launch_tn<128, false>(maps, p, grid, stream);
+  if (tn == 64) return launch_tn<64, false>(maps, p, grid, stream);
+  if (tn == 32) return launch_tn<32, false>(maps, p, grid, stream);
+  if (tn == 16) return launch_tn<16, false>(maps, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

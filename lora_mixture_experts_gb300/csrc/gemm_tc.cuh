@@ -20,7 +20,7 @@ struct alignas(64) GemmMaps {
 struct GemmParams {
   int mode;            // GemmMode
   int K;               // base reduction length
-  int n_mtiles;        // 128-row weight tiles per token tile
+  int n_mtiles;        // weight tiles per token tile (128 rows; 256 on CTA pairs)
   int out_feats;       // valid output features (I, H or N)
   int half_rows;       // gate_up: row offset of the `up` half (= I)
   int r;               // LoRA rank, 0 = no LoRA
@@ -48,11 +48,17 @@ struct GemmParams {
 };
 
 // Launches one GEMM phase (shrink items first, then the main items) as a
-// persistent kernel on `grid` CTAs.  tn is 16, 32, 64, 128 or 256.
+// persistent kernel on up to `grid` work units (CTAs, or CTA pairs for
+// paired tiles), capped at what can be resident at once.  tn is 16, 32, 64,
+// 128 or 256.
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream);
 
 // Dynamic shared memory of the kernel for a token-tile width.
 size_t moe_gemm_smem_bytes(int tn);
+
+// Whether tiles of this width run on CTA pairs (2-SM MMA): then an item
+// covers 256 weight rows (gate_up: 128 features) instead of 128 (64).
+bool moe_gemm_paired(int tn);
 
 }  // namespace moelora

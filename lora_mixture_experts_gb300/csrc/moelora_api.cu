@@ -406,7 +406,8 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
   a.row_w = ws_ptr<float>(ws, p.off_row_w);
   a.pos_of = ws_ptr<int>(ws, p.off_pos_of);
   a.tn = p.tn;
-  a.spi = p.lora ? 128 / p.r : 0;
+  // a shrink item stacks 128 rows of adapters per CTA (two CTAs when paired)
+  a.spi = p.lora ? (moe_gemm_paired(p.tn) ? 256 : 128) / p.r : 0;
   a.tiles = ws_ptr<TileInfo>(ws, p.off_tiles);
   a.shrink = ws_ptr<ShrinkItem>(ws, p.off_shrink);
   a.slot_adapter = ws_ptr<int>(ws, p.off_slot_ad);
@@ -435,9 +436,12 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   return g;
 }
 
+// Work units to launch: at most one per item (the launcher caps it at what
+// can be resident at once).
 int gemm_grid(const Plan& p, int n_mtiles, int sms) {
+  (void)sms;
   const long long items = static_cast<long long>(p.n_sh_max) + static_cast<long long>(p.n_tiles_max) * n_mtiles;
-  return static_cast<int>(std::max<long long>(1, std::min<long long>(items, sms)));
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(items, 1 << 20)));
 }
 
 #define MOELORA_CUDA_CHECK(expr)                 \
@@ -567,7 +571,8 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   GemmParams gu = gemm_params(p, ws, a);
   gu.mode = kModeGateUp;
   gu.K = p.H;
-  gu.n_mtiles = (p.I + 63) / 64;
+  const bool paired = moe_gemm_paired(p.tn);
+  gu.n_mtiles = (p.I + (paired ? 127 : 63)) / (paired ? 128 : 64);
   gu.out_feats = p.I;
   gu.half_rows = p.I;
   gu.done_target = 1;
@@ -579,7 +584,7 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   GemmParams gd = gemm_params(p, ws, a);
   gd.mode = kModeDown;
   gd.K = p.I;
-  gd.n_mtiles = (p.H + 127) / 128;
+  gd.n_mtiles = (p.H + (paired ? 255 : 127)) / (paired ? 256 : 128);
   gd.out_feats = p.H;
   gd.half_rows = 0;
   gd.done_target = 2;
@@ -652,7 +657,8 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
 
   GemmParams g = gemm_params(p, ws, a);
   g.K = p.H;
-  g.n_mtiles = (p.N + 127) / 128;
+  const bool paired = moe_gemm_paired(p.tn);
+  g.n_mtiles = (p.N + (paired ? 255 : 127)) / (paired ? 256 : 128);
   g.out_feats = p.N;
   g.done_target = 1;
   g.group_tiles = group_tiles(p.tn, p.H);

@@ -131,6 +131,8 @@ SMALL = [
     (40, 200, 136, 7, 2, 0, 0),      # no LoRA
     (300, 264, 264, 8, 2, 4, 16),    # several tiles per expert, ragged tail
     (8, 136, 2048, 4, 2, 2, 16),     # few rows per expert, long K: the down phase splits K
+    (600, 256, 200, 2, 1, 3, 32),    # 256-row tiles on CTA pairs, partial tiles and feature blocks
+    (520, 136, 72, 2, 2, 2, 128),    # CTA pairs, rank 128: one adapter per CTA in a shrink item
 ]
 
 
