@@ -15,6 +15,8 @@
 // bit-identical run to run.
 #include "align.cuh"
 
+#include <algorithm>
+
 namespace moelora {
 namespace {
 
@@ -52,10 +54,11 @@ __global__ void __launch_bounds__(kAlignChunk) align_hist_kernel(AlignArgs a) {
   for (int b = tid; b < a.nbins; b += kAlignChunk) out[b] = hist[b];
 }
 
-// Exclusive scan of one value per thread over a 1024-thread block.
+// Exclusive scan of one value per thread over the block (up to 32 warps).
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
   int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -65,7 +68,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = warp_sums[lane];
+    int s = lane < nwarps ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
@@ -75,7 +78,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   }
   __syncthreads();
   const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
-  if (total) *total = warp_sums[31];
+  if (total) *total = warp_sums[nwarps - 1];
   __syncthreads();
   return excl;
 }
@@ -85,7 +88,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 // shared-memory array holding the per-bin entry counts; it is turned into
 // bin starts there (and copied to a.bin_start).  Reading the bins from shared
 // memory keeps the per-expert loops free of global round trips.  Run by all
-// kScanThreads threads of one CTA.
+// threads of one CTA (at least one per expert).
 __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
   const int tid = threadIdx.x;
   const int Lp = a.L + 1;
@@ -120,7 +123,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
       }
     }
   }
-  for (int p = P + tid; p < a.Pmax; p += kScanThreads) {
+  for (int p = P + tid; p < a.Pmax; p += blockDim.x) {
     a.sorted_ids[p] = a.n;
     if (a.row_tok) {
       a.row_tok[p] = -1;
@@ -128,7 +131,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
       a.row_w[p] = 0.0f;
     }
   }
-  for (int blk = P / a.block_m + tid; blk < a.Pmax / a.block_m; blk += kScanThreads)
+  for (int blk = P / a.block_m + tid; blk < a.Pmax / a.block_m; blk += blockDim.x)
     a.blk_expert[blk] = -1;
   if (tid == 0) {
     if (a.seg_off) a.seg_off[a.nbins] = P;
@@ -213,14 +216,22 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
   grid_dependency_trigger();
   const int tid = threadIdx.x;
 
-  // per-bin chunk offsets (in place) and totals
+  // per-bin chunk offsets (in place) and totals; chunks are read eight at a
+  // time so the loads of a bin are in flight together
   for (int b = tid; b < a.nbins; b += kScanThreads) {
     int run = 0;
-    for (int c = 0; c < a.nchunks; ++c) {
-      int* h = a.chunk_hist + static_cast<size_t>(c) * a.nbins + b;
-      const int v = *h;
-      *h = run;
-      run += v;
+    for (int c0 = 0; c0 < a.nchunks; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = c0 + u < a.nchunks ? a.chunk_hist[static_cast<size_t>(c0 + u) * a.nbins + b] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < a.nchunks) {
+          a.chunk_hist[static_cast<size_t>(c0 + u) * a.nbins + b] = run;
+          run += v[u];
+        }
+      }
     }
     sb[b] = run;
   }
@@ -229,9 +240,10 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
 }
 
 // The whole align in one CTA for up to kScanThreads entries (decode-sized
-// batches): bins, stable in-bin ranks (warps take turns in entry order, a
-// warp's lanes are ordered among themselves), totals, the shared tables
-// step, then the scatter.  Same results as hist + scan + scatter.
+// batches), launched with max(entries, experts) threads rounded to a warp:
+// bins, stable in-bin ranks (the warps holding entries take turns in entry
+// order, a warp's lanes are ordered among themselves), totals, the shared
+// tables step, then the scatter.  Same results as hist + scan + scatter.
 __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) {
   __shared__ int warp_sums[32];
   extern __shared__ int sm_bins[];   // [nbins] running counts
@@ -250,10 +262,11 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
     else
       bin = e * (a.L + 1) + l + 1;
   }
-  for (int b = tid; b < a.nbins; b += kScanThreads) sm_bins[b] = 0;
+  for (int b = tid; b < a.nbins; b += blockDim.x) sm_bins[b] = 0;
   __syncthreads();
   int rank = 0;
-  for (int w = 0; w < kScanThreads / 32; ++w) {
+  const int entry_warps = (a.n + 31) >> 5;
+  for (int w = 0; w < entry_warps; ++w) {
     if (warp == w) {
       const unsigned peers = __match_any_sync(0xffffffffu, bin);
       const int leader = __ffs(peers) - 1;
@@ -366,8 +379,9 @@ bool align_small_fits(const AlignArgs& a) {
 }
 
 cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained) {
-  return launch_chained(align_small_kernel, dim3(1), dim3(kScanThreads), a.nbins * sizeof(int),
-                        stream, chained, a);
+  const int threads = (std::max(std::max(a.n, a.E), 32) + 31) / 32 * 32;
+  return launch_chained(align_small_kernel, dim3(1), dim3(threads), a.nbins * sizeof(int), stream,
+                        chained, a);
 }
 
 cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained) {
