@@ -74,6 +74,18 @@ def test_align_edge_cases():
     _check_align(ids, lo, 64, 40, 32)
 
 
+def test_align_large_shapes():
+    g = torch.Generator().manual_seed(9)
+    # more bins than the single-CTA path holds (256 experts x 33 adapter bins)
+    ids = torch.randint(0, 256, (300, 2), generator=g, dtype=torch.int32)
+    lo = torch.randint(-1, 32, (300,), generator=g, dtype=torch.int32)
+    _check_align(ids, lo, 256, 32, 16)
+    # 65536 entries: 256 chunks through the three-kernel path
+    c = small_moe_case(8192, 64, 64, 256, 8, 4, 16, routing="zipf")
+    ids, _, lo = make_routing(c, seed=2)
+    _check_align(ids, lo, 256, 4, 16)
+
+
 def test_align_bad_index_flag():
     ids = torch.tensor([[0, 1], [1, 7]], dtype=torch.int32, device=DEV)
     lo = torch.tensor([0, -1], dtype=torch.int32, device=DEV)
@@ -146,6 +158,22 @@ def test_forward_small_shapes(shape):
     if L == 0:
         d["lora_ids"] = torch.full((T,), -1, dtype=torch.int32, device=DEV)
     _run_parity(d, what=str(shape))
+
+
+def test_forward_many_experts_top8():
+    c = small_moe_case(1024, 128, 192, 64, 8, 4, 16, adapters="zipf", routing="zipf")
+    d = make_moe_case(c, seed=6, device=DEV)
+    rng = np.random.default_rng(3)
+    _run_parity(d, tokens=np.sort(rng.choice(1024, size=64, replace=False)), what="E64 top-8")
+
+
+def test_forward_empty_batch():
+    c = small_moe_case(4, 64, 64, 4, 2, 2, 16)
+    d = make_moe_case(c, seed=0, device=DEV)
+    e = {k: (v[:0] if k in ("x", "topk_ids", "topk_weights", "lora_ids") else v) for k, v in d.items()}
+    out = _gpu_forward(e)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 64)
 
 
 def test_forward_all_one_expert_and_no_adapter():
