@@ -2,4 +2,4 @@
 imported by tests, the smoke check and the benchmark's CPU baseline, never by
 the library)."""
 from .moe_lora_ref import (as_f64, align_ref, moe_lora_forward_ref,  # noqa: F401
-                           moe_lora_linear_ref, silu)
+                           moe_lora_linear_ref, router_topk_ref, silu)

@@ -35,7 +35,8 @@ Pins (tests under ``tests/test_oracle_pins.py``): a hand-derived closed-form
 example, a scalar brute force on tiny shapes, the merged-weight identity
 x(W + AB) = xW + xAB, adapter -1 / B = 0 reducing to the plain MoE, E = 1
 top-1 reducing to a dense two-projection MLP, linearity in the gate weights,
-and the align definition checked by a counting sort and its invariants.
+the align definition checked by a counting sort and its invariants, and the
+router against a two-expert closed form and a library top-k.
 """
 from __future__ import annotations
 
@@ -43,7 +44,7 @@ import numpy as np
 
 __all__ = [
     "as_f64", "align_ref", "moe_lora_forward_ref", "moe_lora_linear_ref",
-    "silu",
+    "router_topk_ref", "silu",
 ]
 
 
@@ -109,6 +110,32 @@ def align_ref(topk_ids, lora_ids, E, L, block_m):
     seg_off[-1] = P
     return {"sorted_ids": sorted_ids, "blk_expert": blk_expert, "seg_off": seg_off,
             "num_post_pad": P}
+
+
+def router_topk_ref(logits, k):
+    """The router step upstream of the layer (multi-LoRA MoE blog, "Implementing
+    multi-LoRA for MoE in vLLM": the routing algorithm sends each token to its
+    most relevant experts, whose outputs are then aggregated).
+
+    Plain definition: p = softmax(logits[t]); the k experts with the largest p
+    are chosen, larger first, the lower expert index first among equal values;
+    their gate weights are p renormalised over the chosen k, i.e. the softmax
+    of the chosen logits.  Softmax is monotonic, so the choice is taken on the
+    logits themselves (the same values and precision the GPU compares).
+    Returns (ids [T,k] int64, weights [T,k] float64)."""
+    logits = np.asarray(logits)
+    T, E = logits.shape
+    if not 1 <= k <= E:
+        raise ValueError("k out of range")
+    ids = np.zeros((T, k), dtype=np.int64)
+    w = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))[:k]
+        ids[t] = order
+        lt = logits[t].astype(np.float64)
+        sel = np.exp(lt[order] - lt.max())
+        w[t] = sel / sel.sum()
+    return ids, w
 
 
 def _lora_delta(X, A, B):

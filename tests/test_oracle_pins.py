@@ -238,8 +238,31 @@ def pin_align(seed=5):
     return bool(ok)
 
 
+def pin_router(seed=6):
+    """Router: closed form for two experts (weights are a logistic of the logit
+    gap), a library top-k (torch.topk over softmax in float64) on continuous
+    logits, ties broken by the lower index, and the invariants."""
+    import torch
+    ok = True
+    ids, w = ref.router_topk_ref(np.array([[0.5, 2.0]], dtype=np.float32), 2)
+    ok &= ids.tolist() == [[1, 0]]
+    ok &= abs(w[0, 0] - 1.0 / (1.0 + math.exp(-1.5))) < 1e-15
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((40, 16)).astype(np.float32)
+    ids, w = ref.router_topk_ref(lg, 4)
+    p = torch.softmax(torch.tensor(lg, dtype=torch.float64), -1)
+    tv, ti = torch.topk(p, 4, -1)
+    ok &= np.array_equal(ids, ti.numpy())
+    ok &= np.abs(w - (tv / tv.sum(-1, keepdim=True)).numpy()).max() < 1e-14
+    ok &= np.allclose(w.sum(1), 1.0) and bool(np.all(np.diff(w, axis=1) <= 0))
+    tie = np.array([[1.0, 3.0, 3.0, 1.0, 3.0]], dtype=np.float32)
+    ok &= ref.router_topk_ref(tie, 3)[0].tolist() == [[1, 2, 4]]
+    ok &= ref.router_topk_ref(tie, 4)[0].tolist() == [[1, 2, 4, 0]]
+    return bool(ok)
+
+
 PINS = [pin_closed_form, pin_brute_force, pin_merged_identity, pin_base_moe,
-        pin_dense_reduction, pin_linearity, pin_align]
+        pin_dense_reduction, pin_linearity, pin_align, pin_router]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
