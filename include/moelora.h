@@ -167,6 +167,42 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x_dev,
                      void* ws_dev, size_t ws_bytes, moelora_stream_t stream);
 
 /*
+ * moe_lora_route -- the router step upstream of the layer: each token's
+ * top-k experts and gate weights from its router logits.
+ * Cited: multi-LoRA MoE blog, "Implementing multi-LoRA for MoE in vLLM" (the
+ * routing algorithm sends each token to its most relevant experts and their
+ * outputs are aggregated).
+ * Definition: p = softmax(logits[t]); the k largest p are chosen, larger
+ * first, the lower expert index first among equal logits (the choice is made
+ * on the fp32 logits themselves); weights = p renormalised over the chosen k
+ * (= softmax of the chosen logits), computed in fp32.
+ *   logits_dev        [T][E] fp32
+ *   topk_ids_dev      [T][k] int32 out
+ *   topk_weights_dev  [T][k] fp32 out
+ * Only d->T, d->k, d->E are read; k <= 32 and E <= 1024 (else
+ * MOELORA_ERR_UNSUPPORTED).  No workspace.
+ */
+int moe_lora_route(const moelora_dims* d, const float* logits_dev, int32_t* topk_ids_dev,
+                   float* topk_weights_dev, moelora_stream_t stream);
+
+/*
+ * moe_lora_forward_routed -- moe_lora_forward with the router step fused in:
+ * takes router logits [T][E] (fp32) instead of topk_ids / topk_weights and
+ * routes on the device (inside the single-CTA align for batches of up to
+ * 1024 routed entries, as a separate kernel before the align above that).
+ * Same workspace as moe_lora_forward (moelora_workspace_bytes); k <= 32,
+ * E <= 1024.  The result is bit-identical to moe_lora_route followed by
+ * moe_lora_forward on the same inputs.
+ */
+int moe_lora_forward_routed(const moelora_dims* d, const moelora_bf16* x_dev,
+                            const float* router_logits_dev, const int32_t* lora_ids_dev,
+                            const moelora_bf16* W_gate_up_dev, const moelora_bf16* W_down_dev,
+                            const moelora_bf16* A_gu_dev, const moelora_bf16* B_gu_dev,
+                            const moelora_bf16* A_d_dev, const moelora_bf16* B_d_dev,
+                            moelora_bf16* out_dev, void* ws_dev, size_t ws_bytes,
+                            moelora_stream_t stream);
+
+/*
  * moe_lora_linear -- dense multi-LoRA linear, the one-expert, top-1,
  * weight-1 degenerate case of the layer with a single projection and no
  * activation: y[t] = x[t] W^T + [a_t>=0] (x[t] A[a_t]^T) B[a_t]^T.

@@ -53,6 +53,8 @@ _SIGS = {
     "moe_lora_align_noalloc": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _I32, _P, _P,
                                               _P, _P, _P]),
     "moe_lora_forward": (ctypes.c_int, [ctypes.POINTER(moelora_dims)] + [_P] * 12 + [_SZ, _P]),
+    "moe_lora_route": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _P, _P]),
+    "moe_lora_forward_routed": (ctypes.c_int, [ctypes.POINTER(moelora_dims)] + [_P] * 11 + [_SZ, _P]),
     "moe_lora_linear": (ctypes.c_int, [ctypes.POINTER(moelora_linear_dims)] + [_P] * 7 + [_SZ, _P]),
     "moelora_set_timing_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _I32]),
     "moelora_last_launch_count": (_I32, []),
@@ -191,6 +193,41 @@ def moe_lora_forward(x, topk_ids, topk_weights, lora_ids, W_gate_up, W_down,
                               _ptr(B_gu), _ptr(A_d), _ptr(B_d), _ptr(out), _ptr(ws), ws.numel(),
                               _stream(stream))
     _check(st, "moe_lora_forward")
+    return out
+
+
+def moe_lora_route(logits, k: int, ids=None, weights=None, stream=None):
+    """Router top-k on device: returns (topk_ids [T,k] int32, topk_weights [T,k] fp32)."""
+    lib = load()
+    T, E = logits.shape
+    d = moelora_dims(T, k, E, 8, 8, 0, 0)
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    st = lib.moe_lora_route(ctypes.byref(d), _ptr(logits), _ptr(ids), _ptr(weights), _stream(stream))
+    _check(st, "moe_lora_route")
+    return ids, weights
+
+
+def moe_lora_forward_routed(x, router_logits, k: int, lora_ids, W_gate_up, W_down,
+                            A_gu=None, B_gu=None, A_d=None, B_d=None, out=None, ws=None,
+                            stream=None):
+    """The layer with the router fused in (router logits [T,E] fp32, top-k)."""
+    lib = load()
+    T, H = x.shape
+    E, two_i, _ = W_gate_up.shape
+    L, r = (A_gu.shape[0], A_gu.shape[2]) if A_gu is not None else (0, 0)
+    d = moelora_dims(T, k, E, H, two_i // 2, L, r)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = alloc_workspace(lib.moelora_workspace_bytes(ctypes.byref(d)), x.device)
+    st = lib.moe_lora_forward_routed(ctypes.byref(d), _ptr(x), _ptr(router_logits), _ptr(lora_ids),
+                                     _ptr(W_gate_up), _ptr(W_down), _ptr(A_gu), _ptr(B_gu),
+                                     _ptr(A_d), _ptr(B_d), _ptr(out), _ptr(ws), ws.numel(),
+                                     _stream(stream))
+    _check(st, "moe_lora_forward_routed")
     return out
 
 

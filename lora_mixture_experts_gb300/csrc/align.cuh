@@ -11,6 +11,12 @@ constexpr int kMaxBins = 11264;         // E*(L+1) held in one CTA's shared memo
 constexpr int kMaxExperts = 1024;
 
 struct AlignArgs {
+  // router (optional): when logits is set, the align first picks each token's
+  // top-k experts from logits [T][E] (fp32) and writes them to
+  // topk_ids_out / topk_w_out, which then serve as topk_ids / topk_weights
+  const float* logits;
+  int32_t* topk_ids_out;
+  float* topk_w_out;
   // inputs
   const int32_t* topk_ids;      // [T*k]; NULL = every entry on expert 0 (E == 1, k == 1)
   const int32_t* lora_ids;      // [T]
@@ -53,6 +59,13 @@ struct AlignArgs {
 cudaError_t launch_align_hist(const AlignArgs& a, cudaStream_t stream, bool chained);
 cudaError_t launch_align_scan(const AlignArgs& a, cudaStream_t stream, bool chained);
 cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained);
+
+// Router: top-k experts of each token from logits [T][E], larger logit first
+// (lower index on ties), gate weights = softmax over the chosen logits.
+// One warp per token; E <= 1024, k <= 32.
+constexpr int kRouteMaxE = 1024;
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                         cudaStream_t stream, bool chained);
 
 // The same align in one single-CTA kernel, for small batches.
 constexpr int kSmallMaxBins = 8192;

@@ -15,12 +15,76 @@
 // bit-identical run to run.
 #include "align.cuh"
 
+#include <cmath>
+
 #include <algorithm>
 
 namespace moelora {
 namespace {
 
 constexpr int kScanThreads = 1024;
+
+// ---------------------------------------------------------------- router
+// Top-k of one token's logits by one warp: k rounds of a warp argmax (larger
+// logit first, lower expert index on ties; NaN never wins), then the gate
+// weights as the softmax of the chosen logits.  Lane j < k keeps expert j.
+__device__ __forceinline__ void route_token(const float* __restrict__ lg, int E, int k,
+                                            int32_t* __restrict__ ids, float* __restrict__ w,
+                                            int lane) {
+  uint32_t taken = 0;          // slot i of this lane <-> expert lane + 32 i
+  int my_id = -1;
+  float my_l = 0.0f;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int i = 0, e = lane; e < E; ++i, e += 32) {
+      if (taken & (1u << i)) continue;
+      const float v = lg[e];
+      if (v > bv || (v == bv && e < be)) {
+        bv = v;
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be != 0x7fffffff && (be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == r) {
+      my_id = be == 0x7fffffff ? -1 : be;
+      my_l = bv;
+    }
+  }
+  // softmax over the chosen logits (round 0 holds the largest)
+  const float m = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = (lane < k && my_id >= 0) ? expf(my_l - m) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    ids[lane] = my_id;
+    w[lane] = ex / sum;
+  }
+}
+
+constexpr int kRouteWarps = 8;
+
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const float* __restrict__ logits,
+                                                                 int T, int E, int k,
+                                                                 int32_t* __restrict__ ids,
+                                                                 float* __restrict__ w) {
+  grid_dependency_wait();
+  grid_dependency_trigger();
+  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  route_token(logits + static_cast<size_t>(t) * E, E, k, ids + static_cast<size_t>(t) * k,
+              w + static_cast<size_t>(t) * k, threadIdx.x & 31);
+}
 
 __global__ void __launch_bounds__(kAlignChunk) align_hist_kernel(AlignArgs a) {
   grid_dependency_wait();
@@ -253,6 +317,14 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int f = tid;
+  if (a.logits) {
+    // router fused in: the CTA's warps pick every token's top-k first
+    for (int t = warp; t < a.T; t += blockDim.x >> 5)
+      route_token(a.logits + static_cast<size_t>(t) * a.E, a.E, a.k,
+                  a.topk_ids_out + static_cast<size_t>(t) * a.k,
+                  a.topk_w_out + static_cast<size_t>(t) * a.k, lane);
+    __syncthreads();
+  }
   int bin = -1;
   if (f < a.n) {
     const int e = a.topk_ids ? a.topk_ids[f] : 0;
@@ -382,6 +454,13 @@ cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool cha
   const int threads = (std::max(std::max(a.n, a.E), 32) + 31) / 32 * 32;
   return launch_chained(align_small_kernel, dim3(1), dim3(threads), a.nbins * sizeof(int), stream,
                         chained, a);
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                         cudaStream_t stream, bool chained) {
+  const int grid = std::max(1, (T + kRouteWarps - 1) / kRouteWarps);
+  return launch_chained(route_kernel, dim3(grid), dim3(kRouteWarps * 32), 0, stream, chained, logits,
+                        T, E, k, ids, w);
 }
 
 cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool chained) {

@@ -37,6 +37,7 @@ struct Plan {
   size_t off_row_tok = 0, off_row_lora = 0, off_row_w = 0, off_pos_of = 0;
   size_t off_tiles = 0, off_shrink = 0, off_slot_ad = 0, off_tile_done = 0;
   size_t off_xperm = 0, off_zgu = 0, off_zd = 0, off_act = 0, off_ypair = 0;
+  size_t off_topk_ids = 0, off_topk_w = 0;   // router results (routed forward)
   size_t total = 0;
 };
 
@@ -165,6 +166,8 @@ Plan plan_forward(const moelora_dims* d) {
   const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
   p.off_zd = b.take(std::max<size_t>(zbytes, 16));
   p.off_act = b.take(static_cast<size_t>(p.Pmax) * p.I * 2);
+  p.off_topk_ids = b.take(static_cast<size_t>(p.n) * 4);
+  p.off_topk_w = b.take(static_cast<size_t>(p.n) * 4);
   p.ksplit = choose_ksplit(expected_tiles(p.T, p.k, p.E, p.tn), (p.H + 127) / 128, p.I,
                            static_cast<double>(p.n) / p.E);
   p.off_ypair = b.take(static_cast<size_t>(p.ksplit) * p.Pmax * p.H * 4);
@@ -355,6 +358,13 @@ cudaError_t run_align(Launcher& ln, const AlignArgs& a, cudaStream_t stream) {
     return launch_align_small(a, stream, false);
   }
   bool first = true;
+  if (a.logits) {
+    ln.before("route");
+    if ((e = launch_route(a.logits, a.T, a.E, a.k, a.topk_ids_out, a.topk_w_out, stream, false)) !=
+        cudaSuccess)
+      return e;
+    first = false;
+  }
   if (a.nchunks > 0) {
     ln.before("align_hist");
     if ((e = launch_align_hist(a, stream, !first)) != cudaSuccess) return e;
@@ -506,17 +516,25 @@ int moe_lora_align(const moelora_dims* d, const int32_t* topk_ids, const int32_t
   return MOELORA_OK;
 }
 
-int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t* topk_ids,
-                     const float* topk_weights, const int32_t* lora_ids,
-                     const moelora_bf16* W_gate_up, const moelora_bf16* W_down,
-                     const moelora_bf16* A_gu, const moelora_bf16* B_gu, const moelora_bf16* A_d,
-                     const moelora_bf16* B_d, moelora_bf16* out, void* ws, size_t ws_bytes,
-                     moelora_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+// The forward, routed by topk_ids/topk_weights or, when logits is set, by the
+// router run on device (fused into the align for small batches).
+int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* topk_ids,
+                 const float* topk_weights, bool routed, const float* logits, const int32_t* lora_ids,
+                 const moelora_bf16* W_gate_up, const moelora_bf16* W_down,
+                 const moelora_bf16* A_gu, const moelora_bf16* B_gu, const moelora_bf16* A_d,
+                 const moelora_bf16* B_d, moelora_bf16* out, void* ws, size_t ws_bytes,
+                 moelora_stream_t stream_) {
   int st = check_moe_dims(d);
   if (st != MOELORA_OK) return st;
+  if (routed && (d->k > 32 || d->E > kRouteMaxE)) return MOELORA_ERR_UNSUPPORTED;
   if (d->T == 0) return MOELORA_OK;
   const bool lora = d->L > 0 && d->r > 0;
-  if (!x || !topk_ids || !topk_weights || !lora_ids || !W_gate_up || !W_down || !out)
+  if (!x || (routed ? !logits : (!topk_ids || !topk_weights)) || !lora_ids || !W_gate_up ||
+      !W_down || !out)
     return MOELORA_ERR_INVALID_ARG;
   if (lora && (!A_gu || !B_gu || !A_d || !B_d)) return MOELORA_ERR_INVALID_ARG;
   if (misaligned(x) || misaligned(W_gate_up) || misaligned(W_down) || misaligned(out))
@@ -536,6 +554,13 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   a.lora_ids = lora_ids;
   a.lora_ignore = p.lora ? 0 : 1;
   a.topk_weights = topk_weights;
+  if (routed) {
+    a.logits = logits;
+    a.topk_ids_out = ws_ptr<int32_t>(ws, p.off_topk_ids);
+    a.topk_w_out = ws_ptr<float>(ws, p.off_topk_w);
+    a.topk_ids = a.topk_ids_out;
+    a.topk_weights = a.topk_w_out;
+  }
   fill_gemm_tables(p, ws, a);
 
   auto* x_perm = ws_ptr<__nv_bfloat16>(ws, p.off_xperm);
@@ -610,6 +635,45 @@ int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t
   MOELORA_CUDA_CHECK(launch_combine(ypair, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
                                     p.k, p.H, p.ksplit, static_cast<long long>(p.Pmax) * p.H, sms,
                                     stream));
+  ln.finish();
+  return MOELORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_lora_forward(const moelora_dims* d, const moelora_bf16* x, const int32_t* topk_ids,
+                     const float* topk_weights, const int32_t* lora_ids,
+                     const moelora_bf16* W_gate_up, const moelora_bf16* W_down,
+                     const moelora_bf16* A_gu, const moelora_bf16* B_gu, const moelora_bf16* A_d,
+                     const moelora_bf16* B_d, moelora_bf16* out, void* ws, size_t ws_bytes,
+                     moelora_stream_t stream) {
+  return forward_impl(d, x, topk_ids, topk_weights, false, nullptr, lora_ids, W_gate_up, W_down,
+                      A_gu, B_gu, A_d, B_d, out, ws, ws_bytes, stream);
+}
+
+int moe_lora_forward_routed(const moelora_dims* d, const moelora_bf16* x,
+                            const float* router_logits, const int32_t* lora_ids,
+                            const moelora_bf16* W_gate_up, const moelora_bf16* W_down,
+                            const moelora_bf16* A_gu, const moelora_bf16* B_gu,
+                            const moelora_bf16* A_d, const moelora_bf16* B_d, moelora_bf16* out,
+                            void* ws, size_t ws_bytes, moelora_stream_t stream) {
+  return forward_impl(d, x, nullptr, nullptr, true, router_logits, lora_ids, W_gate_up, W_down,
+                      A_gu, B_gu, A_d, B_d, out, ws, ws_bytes, stream);
+}
+
+int moe_lora_route(const moelora_dims* d, const float* logits, int32_t* topk_ids,
+                   float* topk_weights, moelora_stream_t stream) {
+  if (!d || d->T < 0 || d->E < 1 || d->k < 1 || d->k > d->E) return MOELORA_ERR_INVALID_ARG;
+  if (d->k > 32 || d->E > kRouteMaxE) return MOELORA_ERR_UNSUPPORTED;
+  if (d->T == 0) return MOELORA_OK;
+  if (!logits || !topk_ids || !topk_weights) return MOELORA_ERR_INVALID_ARG;
+  Launcher ln(reinterpret_cast<cudaStream_t>(stream));
+  ln.before("route");
+  if (launch_route(logits, d->T, d->E, d->k, topk_ids, topk_weights,
+                   reinterpret_cast<cudaStream_t>(stream), false) != cudaSuccess)
+    return MOELORA_ERR_CUDA;
   ln.finish();
   return MOELORA_OK;
 }

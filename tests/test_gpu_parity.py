@@ -253,3 +253,57 @@ def test_linear_small_no_lora_and_ragged():
         exp = ref.moe_lora_linear_ref(n["x"], lo.cpu().numpy(), n["W"], n.get("A"), n.get("B"))
         ok, msg = compare(out, exp, f"linear {(T, K, N, L, r)}")
         assert ok, msg
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("T,E,k", [(16, 32, 4), (300, 64, 6), (5, 1024, 8), (64, 8, 8), (7, 3, 1)])
+def test_route_matches_oracle(T, E, k):
+    g = torch.Generator().manual_seed(T * 131 + E)
+    logits = torch.randn(T, E, generator=g)
+    logits[0, :min(E, 4)] = 0.25            # ties: the lower index wins
+    ids, w = binding.moe_lora_route(logits.to(DEV), k)
+    torch.cuda.synchronize()
+    eids, ew = ref.router_topk_ref(logits.numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), eids)
+    assert np.abs(w.cpu().numpy() - ew).max() < 2e-6
+
+
+def _logits_for(d, E, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(d["x"].shape[0], E, generator=g).to(DEV)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_forward_routed_equals_route_then_forward(name):
+    c = CONFIGS[name]
+    d = make_moe_case(c, seed=0, device=DEV)
+    logits = _logits_for(d, c.E, 5)
+    out_r = binding.moe_lora_forward_routed(d["x"], logits, c.k, d["lora_ids"], d["W_gate_up"],
+                                            d["W_down"], d["A_gu"], d["B_gu"], d["A_d"], d["B_d"])
+    ids, w = binding.moe_lora_route(logits, c.k)
+    out_s = binding.moe_lora_forward(d["x"], ids, w, d["lora_ids"], d["W_gate_up"], d["W_down"],
+                                     d["A_gu"], d["B_gu"], d["A_d"], d["B_d"])
+    torch.cuda.synchronize()
+    assert torch.equal(out_r, out_s)
+    # and against the oracle with the oracle's own routing
+    eids, ew = ref.router_topk_ref(logits.cpu().numpy(), c.k)
+    assert np.array_equal(ids.cpu().numpy(), eids)
+    n = np_inputs(d)
+    exp = ref.moe_lora_forward_ref(n["x"], eids, ew, n["lora_ids"], n["W_gate_up"], n["W_down"],
+                                   n["A_gu"], n["B_gu"], n["A_d"], n["B_d"])
+    ok, msg = compare(out_r, exp, f"routed {name}")
+    assert ok, msg
+
+
+def test_forward_routed_large_batch():
+    # above the single-CTA align: router kernel, then the three align kernels
+    c = small_moe_case(600, 128, 128, 16, 4, 3, 16)
+    d = make_moe_case(c, seed=2, device=DEV)
+    logits = _logits_for(d, c.E, 8)
+    out_r = binding.moe_lora_forward_routed(d["x"], logits, c.k, d["lora_ids"], d["W_gate_up"],
+                                            d["W_down"], d["A_gu"], d["B_gu"], d["A_d"], d["B_d"])
+    ids, w = binding.moe_lora_route(logits, c.k)
+    out_s = binding.moe_lora_forward(d["x"], ids, w, d["lora_ids"], d["W_gate_up"], d["W_down"],
+                                     d["A_gu"], d["B_gu"], d["A_d"], d["B_d"])
+    torch.cuda.synchronize()
+    assert torch.equal(out_r, out_s)
