@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bounded CPU work of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tuning", default=os.path.join(ROOT, "lora_mixture_experts_gb300", "tuning"),
+                    help="tuned launch-choice table (file or folder); 'none' = built-in choices")
     return ap.parse_args()
 
 
@@ -269,6 +271,10 @@ def run_ours(args, rank, world, device):
     from lora_mixture_experts_gb300.inputs import CONFIGS, LinearCase, make_linear_case, make_moe_case
 
     binding.load(build_if_missing=True)
+    tuning = None
+    if args.tuning and args.tuning != "none" and os.path.exists(args.tuning):
+        binding.moelora_load_tuning(args.tuning)
+        tuning = os.path.relpath(args.tuning, ROOT)
     case = CONFIGS[args.config]
     linear = isinstance(case, LinearCase)
     seed = rank_seed(rank)
@@ -407,7 +413,8 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name(case), "tokens_per_step_per_gpu": T,
                    "l2": "weights larger than the 129 MB L2, no flush between steps",
-                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+                   "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "tuning": tuning or "built-in choices"},
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peaks['source']} ({'bf16 sustained' if unit == 'TFLOP/s' else 'HBM copy'})",

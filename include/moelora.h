@@ -218,6 +218,25 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x_dev,
                     moelora_bf16* out_dev, void* ws_dev, size_t ws_bytes,
                     moelora_stream_t stream);
 
+/*
+ * moelora_load_tuning -- load a table of tuned launch choices (host only).
+ * Cited: multi-LoRA MoE blog, "Kernel config tuning" (block sizes and split
+ * factors tuned per workload, loaded by users from a folder of config files).
+ * `path` is a file or a folder (every *.cfg file in it, in name order); NULL
+ * clears the table.  Each line: `moe` or `linear`, then key=value tokens;
+ * shape keys T (value or range lo-hi), k, E, H, I (linear: K, N), L, r must
+ * match when present; choice keys tn (token tile 16/32/64/128/256) and
+ * ksplit (1..4, K splits of the down / linear phase) override the built-in
+ * choice; the first matching line wins; '#' starts a comment.  Workspace
+ * sizes depend on the choice: load the table before sizing workspaces.
+ * Returns MOELORA_ERR_INVALID_ARG for a missing path or a malformed line
+ * (the previous table is then kept).
+ */
+int moelora_load_tuning(const char* path);
+
+/* Number of entries in the loaded tuning table (host only). */
+int32_t moelora_tuning_entries(void);
+
 /* Per-kernel timing hook: when `events` is non-NULL, the next calls record
  * events[i] (cudaEvent_t, created by the caller) on the call's stream before
  * launch i of the call and events[n_launches] after the last launch, for as

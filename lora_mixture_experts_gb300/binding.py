@@ -56,6 +56,8 @@ _SIGS = {
     "moe_lora_route": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _P, _P]),
     "moe_lora_forward_routed": (ctypes.c_int, [ctypes.POINTER(moelora_dims)] + [_P] * 11 + [_SZ, _P]),
     "moe_lora_linear": (ctypes.c_int, [ctypes.POINTER(moelora_linear_dims)] + [_P] * 7 + [_SZ, _P]),
+    "moelora_load_tuning": (ctypes.c_int, [ctypes.c_char_p]),
+    "moelora_tuning_entries": (_I32, []),
     "moelora_set_timing_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _I32]),
     "moelora_last_launch_count": (_I32, []),
     "moelora_last_launch_name": (ctypes.c_char_p, [_I32]),
@@ -246,6 +248,16 @@ def moe_lora_linear(x, lora_ids, W, A=None, B=None, out=None, ws=None, stream=No
                              _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_lora_linear")
     return out
+
+
+def moelora_load_tuning(path) -> None:
+    """Load (or with None clear) the tuned launch-choice table."""
+    p = None if path is None else os.fsencode(path)
+    _check(load().moelora_load_tuning(p), "moelora_load_tuning")
+
+
+def moelora_tuning_entries() -> int:
+    return load().moelora_tuning_entries()
 
 
 def moelora_get_error(ws, stream=None) -> int:

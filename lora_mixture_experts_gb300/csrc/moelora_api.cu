@@ -11,6 +11,13 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <fstream>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include <dirent.h>
+#include <sys/stat.h>
 
 #include "align.cuh"
 #include "gemm_tc.cuh"
@@ -60,6 +67,97 @@ int env_override(const char* name, int lo, int hi) {
   return (x >= lo && x <= hi) ? x : 0;
 }
 
+// ------------------------------------------------------------ tuning table
+// Lines of `key=value` tokens, '#' starts a comment.  The first token is the
+// entry kind (`moe` or `linear`); shape keys T (a value or a range lo-hi),
+// k, E, H, I, K, N, L, r must match when present (absent = any); the choice
+// keys tn (16/32/64/128/256) and ksplit (1..4) override the built-in
+// choice.  The first matching line wins.
+struct TuneEntry {
+  bool linear = false;
+  int t_lo = 0, t_hi = 0x7fffffff;
+  int k = -1, E = -1, H = -1, I = -1, L = -1, r = -1;   // H = K, I = N for linear
+  int tn = 0, ksplit = 0;
+};
+
+std::mutex g_tune_mu;
+std::vector<TuneEntry> g_tune;
+
+bool parse_tune_line(const std::string& line, TuneEntry& e, bool& is_entry) {
+  std::string body = line.substr(0, line.find('#'));
+  std::istringstream in(body);
+  std::string tok;
+  is_entry = false;
+  if (!(in >> tok)) return true;   // blank
+  if (tok == "moe") e.linear = false;
+  else if (tok == "linear") e.linear = true;
+  else return false;
+  is_entry = true;
+  while (in >> tok) {
+    const size_t eq = tok.find('=');
+    if (eq == std::string::npos) return false;
+    const std::string key = tok.substr(0, eq), val = tok.substr(eq + 1);
+    char* end = nullptr;
+    if (key == "T") {
+      const size_t dash = val.find('-');
+      e.t_lo = static_cast<int>(std::strtol(val.c_str(), &end, 10));
+      if (dash == std::string::npos) {
+        e.t_hi = e.t_lo;
+      } else {
+        e.t_hi = static_cast<int>(std::strtol(val.c_str() + dash + 1, &end, 10));
+      }
+      if (e.t_lo < 0 || e.t_hi < e.t_lo) return false;
+      continue;
+    }
+    const long v = std::strtol(val.c_str(), &end, 10);
+    if (!end || *end != '\0' || val.empty()) return false;
+    const int iv = static_cast<int>(v);
+    if (key == "k") e.k = iv;
+    else if (key == "E") e.E = iv;
+    else if (key == "H" || key == "K") e.H = iv;
+    else if (key == "I" || key == "N") e.I = iv;
+    else if (key == "L") e.L = iv;
+    else if (key == "r") e.r = iv;
+    else if (key == "tn") {
+      if (iv != 16 && iv != 32 && iv != 64 && iv != 128 && iv != 256) return false;
+      e.tn = iv;
+    } else if (key == "ksplit") {
+      if (iv < 1 || iv > 4) return false;
+      e.ksplit = iv;
+    } else {
+      return false;
+    }
+  }
+  return true;
+}
+
+int load_tune_file(const std::string& path, std::vector<TuneEntry>& out) {
+  std::ifstream f(path);
+  if (!f) return MOELORA_ERR_INVALID_ARG;
+  std::string line;
+  while (std::getline(f, line)) {
+    TuneEntry e;
+    bool is_entry = false;
+    if (!parse_tune_line(line, e, is_entry)) return MOELORA_ERR_INVALID_ARG;
+    if (is_entry) out.push_back(e);
+  }
+  return MOELORA_OK;
+}
+
+// Choice for a shape from the loaded table (tn, ksplit; 0 = no override).
+void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, int& tn, int& ks) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  for (const TuneEntry& e : g_tune) {
+    if (e.linear != linear || T < e.t_lo || T > e.t_hi) continue;
+    if ((e.k >= 0 && e.k != k) || (e.E >= 0 && e.E != E) || (e.H >= 0 && e.H != H) ||
+        (e.I >= 0 && e.I != I) || (e.L >= 0 && e.L != L) || (e.r >= 0 && e.r != r))
+      continue;
+    if (e.tn) tn = e.tn;
+    if (e.ksplit) ks = e.ksplit;
+    return;
+  }
+}
+
 bool lora_rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
 
 int check_moe_dims(const moelora_dims* d) {
@@ -106,6 +204,9 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   // expert's rows (smaller tiles leave room for more pipeline stages)
   const int avg = (p.n + p.E - 1) / p.E;
   p.tn = avg <= 16 ? 16 : (avg <= 32 ? 32 : (avg <= 64 ? 64 : (avg <= 128 ? 128 : 256)));
+  int t_tn = 0, t_ks = 0;
+  tune_lookup(p.linear, p.T, p.k, p.E, p.H, p.linear ? p.N : p.I, p.L, p.r, t_tn, t_ks);
+  if (t_tn) p.tn = t_tn;
   if (const int f = env_override("MOELORA_TN", 16, 256))
     if (f == 16 || f == 32 || f == 64 || f == 128 || f == 256) p.tn = f;
   p.n_tiles_max = p.n / p.tn + std::min(p.E, std::max(p.n, 1)) + 1;
@@ -147,6 +248,15 @@ int choose_ksplit(double est_tiles, int n_mtiles, int K, double rows_per_expert)
   return eff(2 * items) >= eff(items) ? 2 : 1;
 }
 
+// Largest split count <= want for which every one of the splits of nk K
+// blocks (ceil(nk / s) blocks each) is non-empty.
+int clamp_ksplit(int want, int K) {
+  const int nk = std::max(1, (K + 63) / 64);
+  int s = std::max(1, std::min(want, nk));
+  while (s > 1 && (s - 1) * ((nk + s - 1) / s) >= nk) --s;
+  return s;
+}
+
 // Expected token tiles of a call: experts touched under uniform routing
 // plus the extra tiles of experts with more than tn rows.
 double expected_tiles(int T, int k, int E, int tn) {
@@ -170,6 +280,12 @@ Plan plan_forward(const moelora_dims* d) {
   p.off_topk_w = b.take(static_cast<size_t>(p.n) * 4);
   p.ksplit = choose_ksplit(expected_tiles(p.T, p.k, p.E, p.tn), (p.H + 127) / 128, p.I,
                            static_cast<double>(p.n) / p.E);
+  {
+    int t_tn = 0, t_ks = 0;
+    tune_lookup(false, p.T, p.k, p.E, p.H, p.I, p.L, p.r, t_tn, t_ks);
+    if (t_ks && !env_override("MOELORA_KSPLIT", 1, 4)) p.ksplit = t_ks;
+  }
+  p.ksplit = clamp_ksplit(p.ksplit, p.I);
   p.off_ypair = b.take(static_cast<size_t>(p.ksplit) * p.Pmax * p.H * 4);
   p.total = b.cur;
   return p;
@@ -187,6 +303,12 @@ Plan plan_linear(const moelora_linear_dims* d) {
   plan_gemm_tables(p, b);
   p.ksplit = choose_ksplit(std::ceil(static_cast<double>(p.T) / p.tn), (p.N + 127) / 128, p.H,
                            static_cast<double>(p.T));
+  {
+    int t_tn = 0, t_ks = 0;
+    tune_lookup(true, p.T, 1, 1, p.H, p.N, p.L, p.r, t_tn, t_ks);
+    if (t_ks && !env_override("MOELORA_KSPLIT", 1, 4)) p.ksplit = t_ks;
+  }
+  p.ksplit = clamp_ksplit(p.ksplit, p.H);
   if (p.ksplit > 1)   // split partials in fp32, summed into out by the combine
     p.off_ypair = b.take(static_cast<size_t>(p.ksplit) * p.Pmax * p.N * 4);
   p.total = b.cur;
@@ -756,6 +878,41 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   }
   ln.finish();
   return MOELORA_OK;
+}
+
+int moelora_load_tuning(const char* path) {
+  std::vector<TuneEntry> table;
+  if (path) {
+    struct stat st;
+    if (stat(path, &st) != 0) return MOELORA_ERR_INVALID_ARG;
+    if (S_ISDIR(st.st_mode)) {
+      // every *.cfg file of the folder, in name order
+      DIR* dir = opendir(path);
+      if (!dir) return MOELORA_ERR_INVALID_ARG;
+      std::vector<std::string> names;
+      while (dirent* de = readdir(dir)) {
+        const std::string n = de->d_name;
+        if (n.size() > 4 && n.compare(n.size() - 4, 4, ".cfg") == 0) names.push_back(n);
+      }
+      closedir(dir);
+      std::sort(names.begin(), names.end());
+      for (const std::string& n : names) {
+        const int st2 = load_tune_file(std::string(path) + "/" + n, table);
+        if (st2 != MOELORA_OK) return st2;
+      }
+    } else {
+      const int st2 = load_tune_file(path, table);
+      if (st2 != MOELORA_OK) return st2;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.swap(table);
+  return MOELORA_OK;
+}
+
+int32_t moelora_tuning_entries(void) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  return static_cast<int32_t>(g_tune.size());
 }
 
 int moelora_set_timing_events(void* const* events, int32_t n_events) {

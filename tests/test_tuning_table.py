@@ -1,0 +1,85 @@
+"""The tuned launch-choice table: parsing, matching, folder loading and the
+override reaching the plan (visible on the host through the workspace size,
+which grows with the token tile and the K split)."""
+import os
+
+import pytest
+
+from lora_mixture_experts_gb300 import binding
+from lora_mixture_experts_gb300.binding import MoeLoraError, moelora_dims, moelora_linear_dims
+
+DEC = moelora_dims(16, 4, 32, 2880, 2880, 8, 32)
+
+
+@pytest.fixture(autouse=True)
+def clear_table(lib):
+    binding.moelora_load_tuning(None)
+    yield
+    binding.moelora_load_tuning(None)
+
+
+def _write(tmp_path, name, text):
+    p = tmp_path / name
+    p.write_text(text)
+    return str(p)
+
+
+def test_override_changes_the_plan(tmp_path):
+    base = binding.moelora_workspace_bytes(DEC)
+    binding.moelora_load_tuning(_write(tmp_path, "a.cfg", "moe T=1-64 E=32 ksplit=1   # one split\n"))
+    assert binding.moelora_tuning_entries() == 1
+    ks1 = binding.moelora_workspace_bytes(DEC)
+    binding.moelora_load_tuning(_write(tmp_path, "b.cfg", "moe T=16 k=4 E=32 H=2880 I=2880 L=8 r=32 ksplit=4\n"))
+    ks4 = binding.moelora_workspace_bytes(DEC)
+    assert ks1 < base < ks4                     # the default splits the decode down phase in two
+    binding.moelora_load_tuning(_write(tmp_path, "c.cfg", "moe T=16 tn=256\n"))
+    assert binding.moelora_workspace_bytes(DEC) > base   # wider token tiles: bigger shrink buffers
+
+
+def test_non_matching_lines_are_ignored(tmp_path):
+    base = binding.moelora_workspace_bytes(DEC)
+    binding.moelora_load_tuning(_write(tmp_path, "a.cfg", "moe T=17-99 ksplit=4\nmoe E=64 ksplit=4\nlinear ksplit=4\n"))
+    assert binding.moelora_tuning_entries() == 3
+    assert binding.moelora_workspace_bytes(DEC) == base
+
+
+def test_first_match_wins_and_linear_entries(tmp_path):
+    binding.moelora_load_tuning(_write(tmp_path, "a.cfg", "moe ksplit=1\nmoe ksplit=4\n"))
+    one = binding.moelora_workspace_bytes(DEC)
+    binding.moelora_load_tuning(_write(tmp_path, "b.cfg", "moe ksplit=1\n"))
+    assert binding.moelora_workspace_bytes(DEC) == one
+    lin = moelora_linear_dims(8, 8192, 28672, 32, 16)
+    base = binding.moelora_linear_workspace_bytes(lin)
+    binding.moelora_load_tuning(_write(tmp_path, "c.cfg", "linear T=1-64 K=8192 N=28672 ksplit=1\n"))
+    assert binding.moelora_linear_workspace_bytes(lin) < base      # no fp32 split partials
+
+
+def test_folder_loads_every_cfg_in_name_order(tmp_path):
+    d = tmp_path / "tuned"
+    d.mkdir()
+    (d / "b.cfg").write_text("moe ksplit=4\n")
+    (d / "a.cfg").write_text("# tuned on GB300\nmoe ksplit=1\n\n")
+    (d / "notes.txt").write_text("moe ksplit=3\n")
+    binding.moelora_load_tuning(str(d))
+    assert binding.moelora_tuning_entries() == 2
+    only1 = binding.moelora_workspace_bytes(DEC)
+    binding.moelora_load_tuning(_write(tmp_path, "x.cfg", "moe ksplit=1\n"))
+    assert binding.moelora_workspace_bytes(DEC) == only1         # a.cfg came first
+
+
+@pytest.mark.parametrize("text", ["moe tn=48\n", "moe ksplit=9\n", "attention T=4\n", "moe T=9-3\n", "moe bogus=1\n", "moe T\n"])
+def test_malformed_tables_are_rejected_and_keep_the_old_one(tmp_path, text):
+    binding.moelora_load_tuning(_write(tmp_path, "ok.cfg", "moe ksplit=1\n"))
+    with pytest.raises(MoeLoraError):
+        binding.moelora_load_tuning(_write(tmp_path, "bad.cfg", text))
+    assert binding.moelora_tuning_entries() == 1
+    with pytest.raises(MoeLoraError):
+        binding.moelora_load_tuning(str(tmp_path / "missing.cfg"))
+
+
+def test_shipped_table_parses():
+    path = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    if not os.path.isdir(path):
+        pytest.skip("no shipped table")
+    binding.moelora_load_tuning(path)
+    assert binding.moelora_tuning_entries() > 0
