@@ -219,6 +219,29 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x_dev,
                     moelora_stream_t stream);
 
 /*
+ * moe_lora_merge_adapter -- the merged-weight fast path for batches served by
+ * a single adapter: writes W' = W + B A for adapter `adapter` and every
+ * expert, both projections:
+ *   W_gate_up_out[e] = W_gate_up[e] + B_gu[a][e] A_gu[a][e]   ([2I][H])
+ *   W_down_out[e]    = W_down[e]    + B_d[a][e]  A_d[a][e]    ([H][I])
+ * (fp32 accumulation, one bf16 rounding).  moe_lora_forward with L = 0 on the
+ * merged weights then gives the LoRA layer for tokens of that adapter with no
+ * shrink/expand work: x(W + AB) = xW + xAB.
+ * Cited: the hybrid-attention decoder page, "static LoRA merge"
+ * (merge_and_unload at initialisation removes the LoRA cost at run time), and
+ * the multi-LoRA MoE blog's y = xW + xAB.
+ *   d: E, H, I, L, r (T and k unused); 0 <= adapter < L; r <= 128.
+ *   Outputs are caller-owned device buffers shaped like the inputs; they may
+ *   not alias the inputs.  Run once per adapter switch; no workspace.
+ */
+int moe_lora_merge_adapter(const moelora_dims* d, int32_t adapter,
+                           const moelora_bf16* W_gate_up_dev, const moelora_bf16* W_down_dev,
+                           const moelora_bf16* A_gu_dev, const moelora_bf16* B_gu_dev,
+                           const moelora_bf16* A_d_dev, const moelora_bf16* B_d_dev,
+                           moelora_bf16* W_gate_up_out_dev, moelora_bf16* W_down_out_dev,
+                           moelora_stream_t stream);
+
+/*
  * moelora_load_tuning -- load a table of tuned launch choices (host only).
  * Cited: multi-LoRA MoE blog, "Kernel config tuning" (block sizes and split
  * factors tuned per workload, loaded by users from a folder of config files).

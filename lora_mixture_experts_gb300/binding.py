@@ -56,6 +56,7 @@ _SIGS = {
     "moe_lora_route": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _P, _P, _P, _P]),
     "moe_lora_forward_routed": (ctypes.c_int, [ctypes.POINTER(moelora_dims)] + [_P] * 11 + [_SZ, _P]),
     "moe_lora_linear": (ctypes.c_int, [ctypes.POINTER(moelora_linear_dims)] + [_P] * 7 + [_SZ, _P]),
+    "moe_lora_merge_adapter": (ctypes.c_int, [ctypes.POINTER(moelora_dims), _I32] + [_P] * 8 + [_P]),
     "moelora_load_tuning": (ctypes.c_int, [ctypes.c_char_p]),
     "moelora_tuning_entries": (_I32, []),
     "moelora_set_timing_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _I32]),
@@ -248,6 +249,24 @@ def moe_lora_linear(x, lora_ids, W, A=None, B=None, out=None, ws=None, stream=No
                              _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_lora_linear")
     return out
+
+
+def moe_lora_merge_adapter(adapter: int, W_gate_up, W_down, A_gu, B_gu, A_d, B_d,
+                           W_gate_up_out=None, W_down_out=None, stream=None):
+    """W' = W + B A of one adapter for every expert; returns (W_gate_up', W_down')."""
+    lib = load()
+    E, two_i, H = W_gate_up.shape
+    L, _, r, _ = A_gu.shape
+    d = moelora_dims(0, 1, E, H, two_i // 2, L, r)
+    if W_gate_up_out is None:
+        W_gate_up_out = torch.empty_like(W_gate_up)
+    if W_down_out is None:
+        W_down_out = torch.empty_like(W_down)
+    st = lib.moe_lora_merge_adapter(ctypes.byref(d), adapter, _ptr(W_gate_up), _ptr(W_down),
+                                    _ptr(A_gu), _ptr(B_gu), _ptr(A_d), _ptr(B_d),
+                                    _ptr(W_gate_up_out), _ptr(W_down_out), _stream(stream))
+    _check(st, "moe_lora_merge_adapter")
+    return W_gate_up_out, W_down_out
 
 
 def moelora_load_tuning(path) -> None:

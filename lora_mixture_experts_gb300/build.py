@@ -16,8 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoelora.so")
-SOURCES = ["align_kernels.cu", "gemm_tc.cu", "moelora_api.cu", "align_noalloc.cu"]
-HEADERS = ["common.cuh", "align.cuh", "gemm_tc.cuh"]
+SOURCES = ["align_kernels.cu", "gemm_tc.cu", "moelora_api.cu", "align_noalloc.cu", "merge.cu"]
+HEADERS = ["common.cuh", "align.cuh", "gemm_tc.cuh", "merge.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

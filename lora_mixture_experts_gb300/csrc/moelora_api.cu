@@ -21,6 +21,7 @@
 
 #include "align.cuh"
 #include "gemm_tc.cuh"
+#include "merge.cuh"
 
 using namespace moelora;
 
@@ -876,6 +877,35 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
                                       1, p.N, p.ksplit, static_cast<long long>(p.Pmax) * p.N, sms,
                                       stream));
   }
+  ln.finish();
+  return MOELORA_OK;
+}
+
+int moe_lora_merge_adapter(const moelora_dims* d, int32_t adapter, const moelora_bf16* W_gate_up,
+                           const moelora_bf16* W_down, const moelora_bf16* A_gu,
+                           const moelora_bf16* B_gu, const moelora_bf16* A_d,
+                           const moelora_bf16* B_d, moelora_bf16* W_gate_up_out,
+                           moelora_bf16* W_down_out, moelora_stream_t stream_) {
+  if (!d || d->E < 1 || d->H < 8 || d->I < 8 || d->L < 1 || d->r < 1) return MOELORA_ERR_INVALID_ARG;
+  if (adapter < 0 || adapter >= d->L) return MOELORA_ERR_INVALID_ARG;
+  if (d->r > 128) return MOELORA_ERR_UNSUPPORTED;
+  if (!W_gate_up || !W_down || !A_gu || !B_gu || !A_d || !B_d || !W_gate_up_out || !W_down_out)
+    return MOELORA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t E = d->E, H = d->H, I = d->I, r = d->r, a = adapter;
+  auto bf = [](const moelora_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); };
+  Launcher ln(stream);
+  ln.before("merge_gate_up");
+  // adapter a's [E][...] slices are contiguous in the [L][E][...] LoRA tensors
+  if (launch_merge(bf(W_gate_up), bf(B_gu) + a * E * 2 * I * r, bf(A_gu) + a * E * r * H,
+                   reinterpret_cast<__nv_bfloat16*>(W_gate_up_out), d->E, 2 * d->I, d->H, d->r,
+                   stream) != cudaSuccess)
+    return MOELORA_ERR_CUDA;
+  ln.before("merge_down");
+  if (launch_merge(bf(W_down), bf(B_d) + a * E * H * r, bf(A_d) + a * E * r * I,
+                   reinterpret_cast<__nv_bfloat16*>(W_down_out), d->E, d->H, d->I, d->r,
+                   stream) != cudaSuccess)
+    return MOELORA_ERR_CUDA;
   ln.finish();
   return MOELORA_OK;
 }

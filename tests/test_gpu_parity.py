@@ -126,11 +126,20 @@ def test_forward_prefill_sampled():
     _run_parity(d, tokens=tokens, what="prefill sample")
 
 
-def test_forward_skewed_sampled():
-    d = make_moe_case(CONFIGS["skewed"], seed=0, device=DEV)
-    rng = np.random.default_rng(1)
-    tokens = np.sort(rng.choice(256, size=12, replace=False))
-    _run_parity(d, tokens=tokens, what="skewed sample")
+@pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
+def test_forward_skewed_sampled(tuned):
+    # the tuned table (the launch configuration bench.py times) runs this
+    # workload on paired 256-token tiles with a split down phase
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    binding.moelora_load_tuning(table if tuned else None)
+    try:
+        d = make_moe_case(CONFIGS["skewed"], seed=0, device=DEV)
+        rng = np.random.default_rng(1)
+        tokens = np.sort(rng.choice(256, size=12, replace=False))
+        _run_parity(d, tokens=tokens, what="skewed sample")
+    finally:
+        binding.moelora_load_tuning(None)
 
 
 SMALL = [
@@ -307,3 +316,41 @@ def test_forward_routed_large_batch():
                                      d["A_gu"], d["B_gu"], d["A_d"], d["B_d"])
     torch.cuda.synchronize()
     assert torch.equal(out_r, out_s)
+
+
+# ------------------------------------------------------------------ merged-weight fast path
+@pytest.mark.parametrize("shape", [(4, 136, 72, 3, 16), (2, 256, 512, 4, 64), (1, 264, 200, 2, 128)])
+def test_merge_adapter_weights(shape):
+    E, H, I, L, r = shape
+    c = small_moe_case(8, H, I, E, 1, L, r)
+    d = make_moe_case(c, seed=3, device=DEV)
+    a = L - 1
+    Wgu, Wd = binding.moe_lora_merge_adapter(a, d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"],
+                                             d["A_d"], d["B_d"])
+    torch.cuda.synchronize()
+    n = np_inputs(d)
+    exp_gu = ref.as_f64(n["W_gate_up"]) + np.einsum("ecq,eqh->ech", ref.as_f64(n["B_gu"][a]),
+                                                    ref.as_f64(n["A_gu"][a]))
+    exp_d = ref.as_f64(n["W_down"]) + np.einsum("ehq,eqi->ehi", ref.as_f64(n["B_d"][a]),
+                                                ref.as_f64(n["A_d"][a]))
+    for got, exp in ((Wgu, exp_gu), (Wd, exp_d)):
+        g = got.float().cpu().numpy().astype(np.float64)
+        # one bf16 rounding of the fp32 sum: within 2^-8 relative (+ a tiny absolute floor)
+        assert np.all(np.abs(g - exp) <= 2.0 ** -8 * np.abs(exp) + 1e-6)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_merged_fast_path_matches_lora_layer(name):
+    c = CONFIGS[name]
+    d = make_moe_case(c, seed=1, device=DEV)
+    a = 2
+    d["lora_ids"] = torch.full((c.T,), a, dtype=torch.int32, device=DEV)   # one adapter for the batch
+    Wgu, Wd = binding.moe_lora_merge_adapter(a, d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"],
+                                             d["A_d"], d["B_d"])
+    no_lora = torch.full((c.T,), -1, dtype=torch.int32, device=DEV)
+    out = binding.moe_lora_forward(d["x"], d["topk_ids"], d["topk_weights"], no_lora, Wgu, Wd)
+    torch.cuda.synchronize()
+    n = np_inputs(d)
+    exp = _oracle_forward(n)                # the LoRA layer, every token on adapter a
+    ok, msg = compare(out, exp, f"merged {name}")
+    assert ok, msg
