@@ -402,10 +402,17 @@ __global__ void permute_kernel(const uint4* __restrict__ x, const int* __restric
   }
 }
 
+// Positions of a token's k pairs are read first and all of its k x nsplit
+// partial rows are requested together (independent loads in flight), then
+// summed j-major, split-minor (the fixed order that makes the result
+// deterministic).  Up to kCombineMaxK pairs take this path; more fall back to
+// a loop.
+constexpr int kCombineMaxK = 8;
+
 __global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __restrict__ pos_of,
                                uint2* __restrict__ out, int T, int k, int hv, int nsplit,
                                long long split_stride4) {
-  // hv = H / 4: four features per thread; partials summed j-major, split-minor
+  // hv = H / 4: four features per thread
   grid_dependency_wait();
   grid_dependency_trigger();
   const size_t total = static_cast<size_t>(T) * hv;
@@ -414,15 +421,39 @@ __global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __r
     const int t = static_cast<int>(i / hv);
     const int c = static_cast<int>(i - static_cast<size_t>(t) * hv);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int pos = pos_of[t * k + j];
-      if (pos < 0) continue;
-      for (int s = 0; s < nsplit; ++s) {
-        const float4 v = y_pair[s * split_stride4 + static_cast<size_t>(pos) * hv + c];
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+    if (k <= kCombineMaxK && nsplit <= 2) {
+      int pos[kCombineMaxK];
+#pragma unroll
+      for (int j = 0; j < kCombineMaxK; ++j) pos[j] = j < k ? pos_of[t * k + j] : -1;
+      float4 v[kCombineMaxK][2];
+#pragma unroll
+      for (int j = 0; j < kCombineMaxK; ++j)
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          v[j][s] = (pos[j] >= 0 && s < nsplit)
+                        ? y_pair[s * split_stride4 + static_cast<size_t>(pos[j]) * hv + c]
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kCombineMaxK; ++j)
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (pos[j] < 0 || s >= nsplit) continue;
+          acc.x += v[j][s].x;
+          acc.y += v[j][s].y;
+          acc.z += v[j][s].z;
+          acc.w += v[j][s].w;
+        }
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const int pos = pos_of[t * k + j];
+        if (pos < 0) continue;
+        for (int s = 0; s < nsplit; ++s) {
+          const float4 v = y_pair[s * split_stride4 + static_cast<size_t>(pos) * hv + c];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
       }
     }
     uint2 o;

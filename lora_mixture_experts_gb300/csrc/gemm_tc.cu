@@ -285,7 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
           const int kc0 = it.ks * nks;
           const int nkc = min(nk, kc0 + nks) - kc0;
-          const int rot = k_rotation(it, nkc);
+          // (paired tiles, tensor-bound: the token tiles of one expert read
+          // the same weight blocks at the same time, so no rotation there)
+          const int rot = PAIR ? 0 : k_rotation(it, nkc);
           // this CTA's 128 weight rows: gate_up features m*64*(1+PAIR) + rank*64,
           // down / linear rows m*kMRows + rank*128
           const int grow = gate_up ? it.m * (PAIR ? 128 : 64) + static_cast<int>(rank) * 64
