@@ -388,79 +388,127 @@ __global__ void __launch_bounds__(kAlignChunk) align_scatter_kernel(AlignArgs a)
   }
 }
 
-__global__ void permute_kernel(const uint4* __restrict__ x, const int* __restrict__ row_tok,
-                               uint4* __restrict__ x_perm, int Pmax, int hv) {
+// One warp per (sorted row, chunk of 32 * kPermUnroll 16-byte pieces): the
+// row's token is read once and the lane's pieces are copied with all their
+// loads in flight.  Rows without a token (the per-expert padding and the
+// rows past the padded total) are not written: a tile reads them only into
+// MMA columns that its epilogue drops, and each D column depends on its own
+// token row alone.
+constexpr int kPermUnroll = 4;
+
+__global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ x,
+                                                      const int* __restrict__ row_tok,
+                                                      uint4* __restrict__ x_perm, int Pmax, int hv) {
   grid_dependency_wait();
   grid_dependency_trigger();
-  const size_t total = static_cast<size_t>(Pmax) * hv;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int p = static_cast<int>(i / hv);
-    const int c = static_cast<int>(i - static_cast<size_t>(p) * hv);
+  const int lane = threadIdx.x & 31;
+  const int per_row = (hv + 32 * kPermUnroll - 1) / (32 * kPermUnroll);
+  const long long items = static_cast<long long>(Pmax) * per_row;
+  const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); w < items;
+       w += nw) {
+    const int p = static_cast<int>(w / per_row);
+    const int c0 = static_cast<int>(w - static_cast<long long>(p) * per_row) * 32 * kPermUnroll + lane;
     const int t = row_tok[p];
-    x_perm[i] = t >= 0 ? x[static_cast<size_t>(t) * hv + c] : make_uint4(0, 0, 0, 0);
+    if (t < 0) continue;
+    const uint4* src = x + static_cast<size_t>(t) * hv;
+    uint4* dst = x_perm + static_cast<size_t>(p) * hv;
+    uint4 v[kPermUnroll];
+#pragma unroll
+    for (int u = 0; u < kPermUnroll; ++u) {
+      const int c = c0 + u * 32;
+      if (c < hv) v[u] = __ldg(src + c);
+    }
+#pragma unroll
+    for (int u = 0; u < kPermUnroll; ++u) {
+      const int c = c0 + u * 32;
+      if (c < hv) dst[c] = v[u];
+    }
   }
 }
 
-// Positions of a token's k pairs are read first and all of its k x nsplit
-// partial rows are requested together (independent loads in flight), then
-// summed j-major, split-minor (the fixed order that makes the result
-// deterministic).  Up to kCombineMaxK pairs take this path; more fall back to
-// a loop.
-constexpr int kCombineMaxK = 8;
+// out[t] = sum over the token's k pairs (j ascending) and, inside a pair, its
+// K-split partials (split ascending) of the fp32 rows y_pair[pos_of[t, j]],
+// rounded once to bf16.  One warp per (token, chunk of 32 * kCombUnroll
+// four-feature groups): the token's positions are read once, then all
+// K x NS x kCombUnroll partial loads of a lane are in flight together.  The
+// summation order is fixed, so the result is deterministic.
+constexpr int kCombUnroll = 2;
 
-__global__ void combine_kernel(const float4* __restrict__ y_pair, const int* __restrict__ pos_of,
-                               uint2* __restrict__ out, int T, int k, int hv, int nsplit,
-                               long long split_stride4) {
-  // hv = H / 4: four features per thread
+template <int K, int NS>
+__global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__ y_pair,
+                                                      const int* __restrict__ pos_of,
+                                                      uint2* __restrict__ out, int T, int kk,
+                                                      int nsplit, int hv, long long split_stride4) {
   grid_dependency_wait();
   grid_dependency_trigger();
-  const size_t total = static_cast<size_t>(T) * hv;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / hv);
-    const int c = static_cast<int>(i - static_cast<size_t>(t) * hv);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k <= kCombineMaxK && nsplit <= 2) {
-      int pos[kCombineMaxK];
+  const int k = K > 0 ? K : kk;
+  const int ns = NS > 0 ? NS : nsplit;
+  const int lane = threadIdx.x & 31;
+  const int per_tok = (hv + 32 * kCombUnroll - 1) / (32 * kCombUnroll);
+  const long long items = static_cast<long long>(T) * per_tok;
+  const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); w < items;
+       w += nw) {
+    const int t = static_cast<int>(w / per_tok);
+    const int c0 = static_cast<int>(w - static_cast<long long>(t) * per_tok) * 32 * kCombUnroll + lane;
+    float4 acc[kCombUnroll];
 #pragma unroll
-      for (int j = 0; j < kCombineMaxK; ++j) pos[j] = j < k ? pos_of[t * k + j] : -1;
-      float4 v[kCombineMaxK][2];
+    for (int u = 0; u < kCombUnroll; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (K > 0 && NS > 0) {
+      int pos[K > 0 ? K : 1];
 #pragma unroll
-      for (int j = 0; j < kCombineMaxK; ++j)
+      for (int j = 0; j < K; ++j) pos[j] = pos_of[static_cast<size_t>(t) * K + j];
+      float4 v[K > 0 ? K : 1][NS > 0 ? NS : 1][kCombUnroll];
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
-          v[j][s] = (pos[j] >= 0 && s < nsplit)
-                        ? y_pair[s * split_stride4 + static_cast<size_t>(pos[j]) * hv + c]
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < K; ++j)
 #pragma unroll
-      for (int j = 0; j < kCombineMaxK; ++j)
+        for (int s = 0; s < NS; ++s)
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (pos[j] < 0 || s >= nsplit) continue;
-          acc.x += v[j][s].x;
-          acc.y += v[j][s].y;
-          acc.z += v[j][s].z;
-          acc.w += v[j][s].w;
-        }
+          for (int u = 0; u < kCombUnroll; ++u) {
+            const int c = c0 + u * 32;
+            v[j][s][u] = (pos[j] >= 0 && c < hv)
+                             ? y_pair[s * split_stride4 + static_cast<size_t>(pos[j]) * hv + c]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+#pragma unroll
+          for (int u = 0; u < kCombUnroll; ++u) {
+            acc[u].x += v[j][s][u].x;
+            acc[u].y += v[j][s][u].y;
+            acc[u].z += v[j][s][u].z;
+            acc[u].w += v[j][s][u].w;
+          }
     } else {
       for (int j = 0; j < k; ++j) {
-        const int pos = pos_of[t * k + j];
+        const int pos = pos_of[static_cast<size_t>(t) * k + j];
         if (pos < 0) continue;
-        for (int s = 0; s < nsplit; ++s) {
-          const float4 v = y_pair[s * split_stride4 + static_cast<size_t>(pos) * hv + c];
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-        }
+        for (int s = 0; s < ns; ++s)
+#pragma unroll
+          for (int u = 0; u < kCombUnroll; ++u) {
+            const int c = c0 + u * 32;
+            if (c >= hv) continue;
+            const float4 v = y_pair[s * split_stride4 + static_cast<size_t>(pos) * hv + c];
+            acc[u].x += v.x;
+            acc[u].y += v.y;
+            acc[u].z += v.z;
+            acc[u].w += v.w;
+          }
       }
     }
-    uint2 o;
-    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
-    o2[0] = __floats2bfloat162_rn(acc.x, acc.y);
-    o2[1] = __floats2bfloat162_rn(acc.z, acc.w);
-    out[i] = o;
+#pragma unroll
+    for (int u = 0; u < kCombUnroll; ++u) {
+      const int c = c0 + u * 32;
+      if (c >= hv) continue;
+      uint2 o;
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+      o2[0] = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+      o2[1] = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+      out[static_cast<size_t>(t) * hv + c] = o;
+    }
   }
 }
 
@@ -503,8 +551,9 @@ cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool c
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
                            int Pmax, int H, int num_sms, cudaStream_t stream) {
   const int hv = H / 8;
-  const size_t total = static_cast<size_t>(Pmax) * hv;
-  int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
+  const long long items =
+      static_cast<long long>(Pmax) * ((hv + 32 * kPermUnroll - 1) / (32 * kPermUnroll));
+  int grid = static_cast<int>(std::min<long long>((items + 7) / 8, static_cast<long long>(num_sms) * 8));
   if (grid < 1) grid = 1;
   return launch_chained(permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                         reinterpret_cast<const uint4*>(x), row_tok, reinterpret_cast<uint4*>(x_perm),
@@ -515,12 +564,29 @@ cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16
                            int T, int k, int H, int nsplit, long long split_stride,
                            int num_sms, cudaStream_t stream) {
   const int hv = H / 4;
-  const size_t total = static_cast<size_t>(T) * hv;
-  int grid = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
+  const long long items =
+      static_cast<long long>(T) * ((hv + 32 * kCombUnroll - 1) / (32 * kCombUnroll));
+  int grid = static_cast<int>(std::min<long long>((items + 3) / 4, static_cast<long long>(num_sms) * 8));
   if (grid < 1) grid = 1;
-  return launch_chained(combine_kernel, dim3(grid), dim3(256), 0, stream, true,
-                        reinterpret_cast<const float4*>(y_pair), pos_of, reinterpret_cast<uint2*>(out),
-                        T, k, hv, nsplit, split_stride / 4);
+  auto go = [&](auto kernel) {
+    return launch_chained(kernel, dim3(grid), dim3(128), 0, stream, true,
+                          reinterpret_cast<const float4*>(y_pair), pos_of, reinterpret_cast<uint2*>(out), T,
+                          k, nsplit, hv, split_stride / 4);
+  };
+  if (nsplit == 1) {
+    if (k == 1) return go(combine_kernel<1, 1>);
+    if (k == 2) return go(combine_kernel<2, 1>);
+    if (k == 4) return go(combine_kernel<4, 1>);
+    if (k == 6) return go(combine_kernel<6, 1>);
+    if (k == 8) return go(combine_kernel<8, 1>);
+  } else if (nsplit == 2) {
+    if (k == 1) return go(combine_kernel<1, 2>);
+    if (k == 2) return go(combine_kernel<2, 2>);
+    if (k == 4) return go(combine_kernel<4, 2>);
+    if (k == 6) return go(combine_kernel<6, 2>);
+    if (k == 8) return go(combine_kernel<8, 2>);
+  }
+  return go(combine_kernel<0, 0>);
 }
 
 }  // namespace moelora

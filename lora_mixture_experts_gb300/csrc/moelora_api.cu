@@ -58,8 +58,9 @@ struct Bump {
   }
 };
 
-// Tuning overrides for benchmarking: MOELORA_KSPLIT (1..4) and MOELORA_TN
-// (16, 32, 64, 128, 256).  Read at planning time, so the workspace size and
+// Tuning overrides for benchmarking: MOELORA_KSPLIT (1..4), MOELORA_TN
+// (16, 32, 64, 128, 256) and MOELORA_GROUP_TILES (token tiles per group of
+// the GEMM item order).  Read at planning time, so the workspace size and
 // the call agree; unset means the built-in choice.
 int env_override(const char* name, int lo, int hi) {
   const char* v = std::getenv(name);
@@ -502,10 +503,20 @@ cudaError_t run_align(Launcher& ln, const AlignArgs& a, cudaStream_t stream) {
   return cudaSuccess;
 }
 
-// Token tiles per L2 group: the group's token rows take about 32 MB of L2.
-int group_tiles(int tn, int K) {
-  const long long per_tile = static_cast<long long>(tn) * K * 2;
-  return static_cast<int>(std::max<long long>(1, (32ll << 20) / per_tile));
+// Token tiles per group of the main-item order (inside a group the weight
+// tile m is the slow index and the token tile the fast one).  One tile per
+// group makes the concurrent items of the persistent grid all weight tiles of
+// one to a few consecutive token tiles, so an expert's tiles read each weight
+// tile together while the grid has room for all of them; when one tile's
+// weight tiles alone fill the grid, a group holds the expert's expected tiles
+// so that they still do.  Measured on GB300 against groups sized to 32 MB of
+// L2: 3.5% faster on the prefill batch, 2.3% on the skewed batch, the same on
+// the decode batch; the dense T=512 linear (two tiles of one weight) needs
+// its two tiles in one group or it reads the weights twice.
+int group_tiles(int tn, int n_m, double rows_per_expert, int units) {
+  if (const int f = env_override("MOELORA_GROUP_TILES", 1, 1 << 20)) return f;
+  const int tpe = std::max(1, static_cast<int>(std::ceil(rows_per_expert / tn)));
+  return static_cast<long long>(n_m) * tpe > units ? tpe : 1;
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
@@ -724,7 +735,9 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gu.out_feats = p.I;
   gu.half_rows = p.I;
   gu.done_target = 1;
-  gu.group_tiles = group_tiles(p.tn, p.H);
+  const int units = paired ? sms / 2 : sms;
+  const double rows_per_expert = static_cast<double>(p.n) / p.E;
+  gu.group_tiles = group_tiles(p.tn, gu.n_mtiles, rows_per_expert, units);
   gu.zbuf = zgu;
   gu.out = act;
   gu.out_ld = p.I;
@@ -736,7 +749,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.out_feats = p.H;
   gd.half_rows = 0;
   gd.done_target = 2;
-  gd.group_tiles = group_tiles(p.tn, p.I);
+  gd.group_tiles = group_tiles(p.tn, gd.n_mtiles, rows_per_expert, units);
   gd.zbuf = zd;
   gd.out = nullptr;
   gd.out_f32 = ypair;
@@ -848,7 +861,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   g.n_mtiles = (p.N + (paired ? 255 : 127)) / (paired ? 256 : 128);
   g.out_feats = p.N;
   g.done_target = 1;
-  g.group_tiles = group_tiles(p.tn, p.H);
+  g.group_tiles = group_tiles(p.tn, g.n_mtiles, static_cast<double>(p.T), paired ? sms / 2 : sms);
   g.zbuf = z;
   g.out_ld = p.N;
   g.ksplit = p.ksplit;
