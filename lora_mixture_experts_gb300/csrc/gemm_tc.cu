@@ -24,7 +24,8 @@
 // KB consecutive 64-wide K blocks (KB = 4 for 16-row token tiles, 2 for 32
 // and 64, 1 above): at decode sizes, where the weights stream from HBM, big
 // stages (64 KB of weights per barrier round trip) read markedly faster than
-// 16 KB ones.  The LoRA expand chunks of up to KB adapters share a stage.
+// 16 KB ones.  The LoRA expand chunks (r-wide, r <= 64) are packed into a
+// stage by bytes: KB * 64 / r of them share one barrier round trip.
 //
 // 256-token tiles run on CTA pairs (2-SM MMA): the two CTAs of a cluster
 // share every item, each loading its 128 weight rows and half of the token
@@ -66,6 +67,14 @@ struct Cfg {
   // shared-memory offset of K block j's A / B tile inside a stage
   __host__ __device__ static constexpr int a_off(int j) { return j * kATileBytes; }
   __host__ __device__ static constexpr int b_off(int j) { return kKB * kATileBytes + j * kBTileBytes; }
+  // LoRA expand chunk j of width lw (16, 32 or 64) packed in a stage: its
+  // 128 B rows in the A region, its up-to-kRowsB z rows in the B region
+  // (kKB * 64 / lw chunks per stage; chunk sizes are multiples of the
+  // swizzle atom, so every chunk starts on one)
+  __host__ __device__ static constexpr int lora_a_off(int j, int lw) { return j * 128 * lw * 2; }
+  __host__ __device__ static constexpr int lora_b_off(int j, int lw) {
+    return kKB * kATileBytes + j * kRowsB * lw * 2;
+  }
 };
 
 struct Item {
@@ -325,8 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lw = p.lora_w;
             const int nl = ti.nslots * p.lora_chunks;   // expand chunks: (slot, chunk) pairs
             const uint32_t per_sub = (PAIR ? 2 : 1) * (128 * lw * 2 + brows * lw * 2);
-            for (int i0 = 0; i0 < nl && ok; i0 += C::kKB, ++cnt) {
-              const int nsub = min(C::kKB, nl - i0);
+            const int cps = C::kKB * 64 / lw;           // chunks packed per stage
+            for (int i0 = 0; i0 < nl && ok; i0 += cps, ++cnt) {
+              const int nsub = min(cps, nl - i0);
               const int s = cnt % C::kStages;
               uint32_t fb;
               if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
@@ -337,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c = (i0 + j) - sl * p.lora_chunks;
                 const int a = p.slot_adapter[ti.slot_base + sl];
                 if (gate_up)
-                  load5(st + C::a_off(j), &maps.lb, fb, c * lw, grow, 0, ti.expert, a);
+                  load5(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, 0, ti.expert, a);
                 else
-                  load4(st + C::a_off(j), &maps.lb, fb, c * lw, grow, ti.expert, a);
-                load2(st + C::b_off(j), tz, fb, c * lw,
+                  load4(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, ti.expert, a);
+                load2(st + C::lora_b_off(j, lw), tz, fb, c * lw,
                       (ti.slot_base + sl) * TN + static_cast<int>(rank) * nh);
               }
             }
@@ -395,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks : 0;
         const int nb = it.shrink ? nk : min(nk, (it.ks + 1) * nks) - it.ks * nks;
         const int st_base = (nb + C::kKB - 1) / C::kKB;
-        const int st_all = st_base + (nl + C::kKB - 1) / C::kKB;
+        const int cps = p.r > 0 ? C::kKB * 64 / p.lora_w : 1;   // expand chunks per stage
+        const int st_all = st_base + (nl + cps - 1) / cps;
         bool first = true;
         for (int sti = 0; sti < st_all; ++sti, ++cnt) {
           const int s = cnt % C::kStages;
@@ -405,14 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = smem_u32(smem + s * C::kStageBytes);
           const bool base = sti < st_base;
           const int nsub = base ? min(C::kKB, nb - sti * C::kKB)
-                                : min(C::kKB, nl - (sti - st_base) * C::kKB);
+                                : min(cps, nl - (sti - st_base) * cps);
           const int width = base ? 64 : p.lora_w;
           const uint32_t swz = base ? 2u : static_cast<uint32_t>(p.lora_swz);
           const uint32_t sbo = base ? 1024u : static_cast<uint32_t>(8 * p.lora_w * 2);
           for (int j = 0; j < nsub; ++j) {
             for (int kk = 0; kk < width / 16; ++kk) {
-              const uint64_t ad = make_smem_desc(st + C::a_off(j) + kk * 32, sbo, swz);
-              const uint64_t bd = make_smem_desc(st + C::b_off(j) + kk * 32, sbo, swz);
+              const uint32_t ao = base ? C::a_off(j) : C::lora_a_off(j, width);
+              const uint32_t bo = base ? C::b_off(j) : C::lora_b_off(j, width);
+              const uint64_t ad = make_smem_desc(st + ao + kk * 32, sbo, swz);
+              const uint64_t bd = make_smem_desc(st + bo + kk * 32, sbo, swz);
               if (PAIR)
                 mma_bf16_pair(d_tmem, ad, bd, idesc, first ? 0u : 1u);
               else

@@ -550,8 +550,14 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
   a.row_w = ws_ptr<float>(ws, p.off_row_w);
   a.pos_of = ws_ptr<int>(ws, p.off_pos_of);
   a.tn = p.tn;
-  // a shrink item stacks 128 rows of adapters per CTA (two CTAs when paired)
-  a.spi = p.lora ? (moe_gemm_paired(p.tn) ? 256 : 128) / p.r : 0;
+  // a shrink item stacks up to 128 rows of adapters per CTA (two CTAs when
+  // paired).  Unpaired (weight-streaming) tiles take fewer: a shrink item
+  // then reads no more LoRA A bytes than a K-split main item reads weight
+  // bytes, so the shrink items (which the main items' expand waits for) are
+  // not the long pole -- with 8 adapters of r=16 over K=8192 one stacked
+  // item streamed 2 MB while every main item streamed 1 MB.
+  const bool paired = moe_gemm_paired(p.tn);
+  a.spi = p.lora ? (paired ? 256 / p.r : std::max(1, 128 / (p.r * p.ksplit))) : 0;
   a.tiles = ws_ptr<TileInfo>(ws, p.off_tiles);
   a.shrink = ws_ptr<ShrinkItem>(ws, p.off_shrink);
   a.slot_adapter = ws_ptr<int>(ws, p.off_slot_ad);
