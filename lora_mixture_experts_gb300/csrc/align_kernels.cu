@@ -270,6 +270,8 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
     a.hdr->n_tiles = tot_t;
     a.hdr->n_slots = tot_s;
     a.hdr->n_shrink = tot_h;
+    a.hdr->work[0] = 0;
+    a.hdr->work[1] = 0;
   }
 }
 

@@ -39,7 +39,8 @@ struct WsHeader {
   int n_tiles;       // token tiles
   int n_slots;       // LoRA slots
   int n_shrink;      // shrink items
-  int pad_[27];
+  int work[2];       // items claimed so far by each GEMM phase (zeroed by the align)
+  int pad_[25];
 };
 
 constexpr int kStatusBadIndex = MOELORA_ERR_BAD_INDEX;

@@ -46,7 +46,19 @@
 namespace moelora {
 namespace {
 
-constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kThreads = 224;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warp 6 items
+constexpr int kSchedWarp = 6;
+constexpr int kQ = 8;                    // item ring slots
+constexpr int kClaimAhead = 1;           // items claimed beyond those the producer has started
+
+// One entry of the item ring: the item index (-1 = no more items) and its
+// token tile, written by the scheduling warp for the producer, MMA and
+// epilogue warps of the CTA.
+struct RingEntry {
+  int w;
+  int pad_[3];
+  TileInfo ti;
+};
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
 constexpr int kXchgStride = 17;          // floats per row of a gate/up exchange buffer
 
@@ -61,8 +73,9 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;
   static constexpr int kXchgBytes = 2 * 64 * kXchgStride * 4;   // gate and up halves
   static constexpr int kBarOff = kStages * kStageBytes + kXchgBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;
-  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+  static constexpr int kNumBars = 2 * kStages + 5 + 3 * kQ;
+  static constexpr int kRingOff = kBarOff + kNumBars * 8 + 16;   // RingEntry[kQ]
+  static constexpr int kSmemBytes = 1024 + kRingOff + kQ * static_cast<int>(sizeof(RingEntry));
   static constexpr int kMRows = PAIR ? 256 : 128;   // weight rows of one item
   // shared-memory offset of K block j's A / B tile inside a stage
   __host__ __device__ static constexpr int a_off(int j) { return j * kATileBytes; }
@@ -164,8 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accf_bar = bars + 2 * C::kStages;       // [2]
   uint64_t* acce_bar = bars + 2 * C::kStages + 2;   // [2]
   uint64_t* drain_bar = bars + 2 * C::kStages + 4;
+  uint64_t* itemf_bar = bars + 2 * C::kStages + 5;   // [kQ] ring entry written
+  uint64_t* iteme_bar = itemf_bar + kQ;              // [kQ] ring entry read by every consumer
+  uint64_t* itemp_bar = iteme_bar + kQ;              // [kQ] ring entry taken by the producer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  RingEntry* ring = reinterpret_cast<RingEntry*>(smem + C::kRingOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -185,6 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&acce_bar[b]), PAIR ? 8 : 4);   // epilogue warps of both CTAs
     }
     mbar_init(smem_u32(drain_bar), 1);
+    // consumers of a ring entry: producer, MMA issuer (leader only), four epilogue warps
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(smem_u32(&itemf_bar[q]), 1);
+      mbar_init(smem_u32(&iteme_bar[q]), leader ? 6 : 5);
+      mbar_init(smem_u32(&itemp_bar[q]), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -221,18 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // shrink completions a tile's item waits for: every CTA of the item signals
   const int done_scale = PAIR ? 2 : 1;
 
+  // Consume ring entry qc (single-thread consumers: producer, MMA issuer):
+  // wait until it is written, copy it, release the slot.
+  auto ring_take = [&](uint32_t qc, int& w, TileInfo& ti, bool producer) -> bool {
+    const int q = static_cast<int>(qc % kQ);
+    if (!mbar_wait(smem_u32(&itemf_bar[q]), (qc / kQ) & 1, abort_flag)) return false;
+    w = ring[q].w;
+    ti = ring[q].ti;
+    mbar_arrive(smem_u32(&iteme_bar[q]));
+    if (producer) mbar_arrive(smem_u32(&itemp_bar[q]));
+    return true;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t cnt = 0;
       bool ok = true;
-      // the next item's table entries are loaded one item ahead
-      Item it_next{};
-      TileInfo ti_next{};
-      if (unit < n_items) {
-        it_next = decode_item(unit, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-        ti_next = p.tiles[it_next.tile];
-      }
       // one TMA load into this CTA's shared memory, counted on the leader's
       // full barrier when paired
       auto load2 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y) {
@@ -255,13 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fb = PAIR ? mapa_shared(smem_u32(&full_bar[s]), 0) : smem_u32(&full_bar[s]);
         return true;
       };
-      for (int w = unit; w < n_items && ok; w += n_units) {
-        const Item it = it_next;
-        const TileInfo ti = ti_next;
-        if (w + n_units < n_items) {
-          it_next = decode_item(w + n_units, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-          ti_next = p.tiles[it_next.tile];
-        }
+      for (uint32_t qc = 0; ok; ++qc) {
+        int w;
+        TileInfo ti;
+        if (!(ok = ring_take(qc, w, ti, true))) break;
+        if (w < 0) break;
+        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
         const int nmma = (ti.nrows + 15) & ~15;
         const int nh = PAIR ? nmma / 2 : nmma;          // token rows this CTA loads
         const int bi = box_index(nh);
@@ -382,19 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t li = 0;
       bool ok = true;
       bool issued = false;
-      Item it_next{};
-      TileInfo ti_next{};
-      if (unit < n_items) {
-        it_next = decode_item(unit, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-        ti_next = p.tiles[it_next.tile];
-      }
-      for (int w = unit; w < n_items && ok; w += n_units, ++li) {
-        const Item it = it_next;
-        const TileInfo ti = ti_next;
-        if (w + n_units < n_items) {
-          it_next = decode_item(w + n_units, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-          ti_next = p.tiles[it_next.tile];
-        }
+      for (uint32_t qc = 0; ok; ++qc, ++li) {
+        int w;
+        TileInfo ti;
+        if (!(ok = ring_take(qc, w, ti, false))) break;
+        if (w < 0) break;
+        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
         const int nmma = (ti.nrows + 15) & ~15;
         const uint32_t idesc = make_idesc_bf16(nmma, PAIR ? 256 : 128);
         const int buf = li & 1;
@@ -452,6 +472,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (globaltimer_ns() - t0 > kWaitLimitNs) break;
       }
     }
+  } else if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ item scheduler
+    // Writes the CTA's item sequence into the ring.  Unpaired tiles claim
+    // items from the launch's counter as they go: items cost about the same,
+    // but SMs stream from HBM at different rates, and a fixed share leaves
+    // the slowest SMs the tail.  Paired tiles keep the fixed round-robin
+    // share (both CTAs of a pair must see the same items).  Items are claimed
+    // in index order, so shrink items are always claimed before the main
+    // items that wait for them.
+    if (lane == 0) {
+      const bool dyn = !PAIR && p.work_ctr != nullptr;
+      bool ok = true;
+      for (uint32_t qp = 0;; ++qp) {
+        const int q = static_cast<int>(qp % kQ);
+        if (!(ok = mbar_wait(smem_u32(&iteme_bar[q]), ((qp / kQ) & 1) ^ 1, abort_flag))) break;
+        // claim no further ahead than kClaimAhead items past the producer, so
+        // that the items left go to whichever CTA runs out first
+        if (qp >= static_cast<uint32_t>(kClaimAhead)) {
+          const uint32_t e = qp - kClaimAhead;
+          if (!(ok = mbar_wait(smem_u32(&itemp_bar[e % kQ]), (e / kQ) & 1, abort_flag))) break;
+        }
+        int w = dyn ? atomicAdd(p.work_ctr, 1) : unit + static_cast<int>(qp) * n_units;
+        if (w >= n_items) w = -1;
+        if (w >= 0) ring[q].ti = p.tiles[decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink).tile];
+        ring[q].w = w;
+        mbar_arrive(smem_u32(&itemf_bar[q]));
+        if (w < 0) break;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        flag_error(p.err, kStatusTimeout);
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
@@ -459,9 +512,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the MMA issuer's "accumulator free" barrier (the leader's, when paired)
     const uint32_t acce0 = PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : smem_u32(&acce_bar[0]);
     uint32_t li = 0;
-    for (int w = unit; w < n_items; w += n_units, ++li) {
+    for (uint32_t qc = 0;; ++qc, ++li) {
+      // the next ring entry: every epilogue thread reads it, the warps agree
+      // on the outcome of the wait, and each warp releases the slot
+      const int q = static_cast<int>(qc % kQ);
+      const bool got = mbar_wait(smem_u32(&itemf_bar[q]), (qc / kQ) & 1, abort_flag);
+      if (bar_red_or(1, 128, !got || *abort_flag)) {
+        if (!got) flag_error(p.err, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      const int w = ring[q].w;
+      const TileInfo ti = ring[q].ti;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&iteme_bar[q]));
+      if (w < 0) break;
       const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
-      const TileInfo ti = p.tiles[it.tile];
       const int nmma = (ti.nrows + 15) & ~15;
       const int buf = li & 1;
       const bool ok = mbar_wait(smem_u32(&accf_bar[buf]), (li >> 1) & 1, abort_flag);

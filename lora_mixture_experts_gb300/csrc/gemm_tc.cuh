@@ -45,6 +45,7 @@ struct GemmParams {
   __nv_bfloat16* out;   // act [Pmax][I] (gate_up) or out [T][N] (linear)
   float* out_f32;       // y_pair [Pmax][H] (down): gate-weighted expert output, fp32
   int out_ld;
+  int* work_ctr;        // items claimed so far (zeroed by the align); NULL = fixed shares
 };
 
 // Launches one GEMM phase (shrink items first, then the main items) as a

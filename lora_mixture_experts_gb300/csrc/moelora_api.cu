@@ -747,6 +747,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gu.zbuf = zgu;
   gu.out = act;
   gu.out_ld = p.I;
+  gu.work_ctr = &a.hdr->work[0];
 
   GemmParams gd = gemm_params(p, ws, a);
   gd.mode = kModeDown;
@@ -762,6 +763,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.ksplit = p.ksplit;
   gd.split_stride = static_cast<long long>(p.Pmax) * p.H;
   gd.out_ld = p.H;
+  gd.work_ctr = &a.hdr->work[1];
 
   Launcher ln(stream);
   MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
@@ -870,6 +872,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   g.group_tiles = group_tiles(p.tn, g.n_mtiles, static_cast<double>(p.T), paired ? sms / 2 : sms);
   g.zbuf = z;
   g.out_ld = p.N;
+  g.work_ctr = &a.hdr->work[0];
   g.ksplit = p.ksplit;
   float* partial = p.ksplit > 1 ? ws_ptr<float>(ws, p.off_ypair) : nullptr;
   if (p.ksplit > 1) {
