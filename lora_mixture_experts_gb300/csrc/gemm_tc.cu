@@ -427,33 +427,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st_base = (nb + C::kKB - 1) / C::kKB;
         const int cps = p.r > 0 ? C::kKB * 64 / p.lora_w : 1;   // expand chunks per stage
         const int st_all = st_base + (nl + cps - 1) / cps;
-        bool first = true;
+        uint32_t acc = 0;   // the item's first MMA overwrites the accumulator
+        // The issuing thread blocks on each MMA (the queue holds about one),
+        // so the work between two MMAs is kept small: descriptors of a stage
+        // are a base plus constant offsets (the 14-bit start field of a
+        // descriptor is the byte address / 16, and every operand of the
+        // shared-memory window stays inside it), and full base stages run
+        // an unrolled loop.
         for (int sti = 0; sti < st_all; ++sti, ++cnt) {
           const int s = cnt % C::kStages;
           const uint32_t ph = (cnt / C::kStages) & 1;
-          if (!(ok = mbar_wait(smem_u32(&full_bar[s]), ph, abort_flag))) break;
+          if (!mbar_try_wait(smem_u32(&full_bar[s]), ph) &&
+              !(ok = mbar_wait(smem_u32(&full_bar[s]), ph, abort_flag)))
+            break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-          const bool base = sti < st_base;
-          const int nsub = base ? min(C::kKB, nb - sti * C::kKB)
-                                : min(cps, nl - (sti - st_base) * cps);
-          const int width = base ? 64 : p.lora_w;
-          const uint32_t swz = base ? 2u : static_cast<uint32_t>(p.lora_swz);
-          const uint32_t sbo = base ? 1024u : static_cast<uint32_t>(8 * p.lora_w * 2);
-          for (int j = 0; j < nsub; ++j) {
-            for (int kk = 0; kk < width / 16; ++kk) {
-              const uint32_t ao = base ? C::a_off(j) : C::lora_a_off(j, width);
-              const uint32_t bo = base ? C::b_off(j) : C::lora_b_off(j, width);
-              const uint64_t ad = make_smem_desc(st + ao + kk * 32, sbo, swz);
-              const uint64_t bd = make_smem_desc(st + bo + kk * 32, sbo, swz);
-              if (PAIR)
-                mma_bf16_pair(d_tmem, ad, bd, idesc, first ? 0u : 1u);
-              else
-                mma_bf16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
-              first = false;
-              issued = true;
+          if (sti < st_base) {   // base GEMM: K blocks of 64 (4 MMAs of K=16 each)
+            const uint64_t ad0 = make_smem_desc(st + C::a_off(0), 1024u, 2u);
+            const uint64_t bd0 = make_smem_desc(st + C::b_off(0), 1024u, 2u);
+            const int nsub = min(C::kKB, nb - sti * C::kKB);
+            if (nsub == C::kKB) {
+#pragma unroll
+              for (int j = 0; j < C::kKB; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t ad = ad0 + static_cast<uint64_t>((C::a_off(j) + kk * 32) >> 4);
+                  const uint64_t bd = bd0 + static_cast<uint64_t>((j * C::kBTileBytes + kk * 32) >> 4);
+                  if (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, acc); else mma_bf16(d_tmem, ad, bd, idesc, acc);
+                  acc = 1;
+                }
+              }
+            } else {
+              for (int j = 0; j < nsub; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t ad = ad0 + static_cast<uint64_t>((C::a_off(j) + kk * 32) >> 4);
+                  const uint64_t bd = bd0 + static_cast<uint64_t>((j * C::kBTileBytes + kk * 32) >> 4);
+                  if (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, acc); else mma_bf16(d_tmem, ad, bd, idesc, acc);
+                  acc = 1;
+                }
+              }
+            }
+          } else {   // LoRA expand: chunks of width lora_w packed by bytes
+            const int lw = p.lora_w;
+            const uint32_t swz = static_cast<uint32_t>(p.lora_swz);
+            const uint32_t sbo = static_cast<uint32_t>(8 * lw * 2);
+            const int nsub = min(cps, nl - (sti - st_base) * cps);
+            for (int j = 0; j < nsub; ++j) {
+              for (int kk = 0; kk < lw / 16; ++kk) {
+                const uint64_t ad = make_smem_desc(st + C::lora_a_off(j, lw) + kk * 32, sbo, swz);
+                const uint64_t bd = make_smem_desc(st + C::lora_b_off(j, lw) + kk * 32, sbo, swz);
+                if (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, acc); else mma_bf16(d_tmem, ad, bd, idesc, acc);
+                acc = 1;
+              }
             }
           }
+          issued = true;
           if (PAIR) mma_commit_pair(smem_u32(&empty_bar[s])); else mma_commit(smem_u32(&empty_bar[s]));
         }
         if (ok) {
