@@ -279,9 +279,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stage s of this CTA is free: wait on its empty barrier; the barrier
       // that counts the stage's bytes is the leader's full barrier
       auto acquire = [&](int s, uint32_t ph, uint32_t& fb) -> bool {
-        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag)) return false;
+        if (!mbar_try_wait(smem_u32(&empty_bar[s]), ph ^ 1) &&
+            !mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))
+          return false;
         fb = PAIR ? mapa_shared(smem_u32(&full_bar[s]), 0) : smem_u32(&full_bar[s]);
         return true;
+      };
+      // stage and phase of stage count cnt, kept running (no division)
+      int sidx = 0;
+      uint32_t sph = 0;
+      auto advance = [&]() {
+        ++cnt;
+        if (++sidx == C::kStages) {
+          sidx = 0;
+          sph ^= 1;
+        }
       };
       for (uint32_t qc = 0; ok; ++qc) {
         int w;
@@ -302,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ns1 = PAIR ? max(0, si.nslot - spc) : 0;
           const int ns_me = rank == 0 ? ns0 : ns1;
           const uint32_t per_kb = (ns0 + ns1) * p.r * 128 + (PAIR ? 2 : 1) * brows * 128;
-          for (int kb0 = 0; kb0 < nk && ok; kb0 += C::kKB, ++cnt) {
+          for (int kb0 = 0; kb0 < nk && ok; kb0 += C::kKB, advance()) {
             const int nkb = min(C::kKB, nk - kb0);
-            const int s = cnt % C::kStages;
+            const int s = sidx;
             uint32_t fb;
-            if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
+            if (!(ok = acquire(s, sph, fb))) break;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
             if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
@@ -328,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // down / linear rows m*kMRows + rank*128
           const int grow = gate_up ? it.m * (PAIR ? 128 : 64) + static_cast<int>(rank) * 64
                                    : it.m * C::kMRows + static_cast<int>(rank) * 128;
-          for (int i0 = 0; i0 < nkc && ok; i0 += C::kKB, ++cnt) {
+          for (int i0 = 0; i0 < nkc && ok; i0 += C::kKB, advance()) {
             const int nkb = min(C::kKB, nkc - i0);
-            const int s = cnt % C::kStages;
+            const int s = sidx;
             uint32_t fb;
-            if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
+            if (!(ok = acquire(s, sph, fb))) break;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
             if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
@@ -362,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nl = ti.nslots * p.lora_chunks;   // expand chunks: (slot, chunk) pairs
             const uint32_t per_sub = (PAIR ? 2 : 1) * (128 * lw * 2 + brows * lw * 2);
             const int cps = C::kKB * 64 / lw;           // chunks packed per stage
-            for (int i0 = 0; i0 < nl && ok; i0 += cps, ++cnt) {
+            for (int i0 = 0; i0 < nl && ok; i0 += cps, advance()) {
               const int nsub = min(cps, nl - i0);
-              const int s = cnt % C::kStages;
+              const int s = sidx;
               uint32_t fb;
-              if (!(ok = acquire(s, (cnt / C::kStages) & 1, fb))) break;
+              if (!(ok = acquire(s, sph, fb))) break;
               const uint32_t st = smem_u32(smem + s * C::kStageBytes);
               if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nsub * per_sub);
               for (int j = 0; j < nsub; ++j) {
@@ -405,7 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      uint32_t cnt = 0;
+      int sidx = 0;            // stage of the next MMA batch, and its full-barrier phase
+      uint32_t sph = 0;
+      const uint32_t smem0 = smem_u32(smem);
       uint32_t li = 0;
       bool ok = true;
       bool issued = false;
@@ -434,14 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // descriptor is the byte address / 16, and every operand of the
         // shared-memory window stays inside it), and full base stages run
         // an unrolled loop.
-        for (int sti = 0; sti < st_all; ++sti, ++cnt) {
-          const int s = cnt % C::kStages;
-          const uint32_t ph = (cnt / C::kStages) & 1;
+        for (int sti = 0; sti < st_all; ++sti) {
+          const int s = sidx;
+          const uint32_t ph = sph;
           if (!mbar_try_wait(smem_u32(&full_bar[s]), ph) &&
               !(ok = mbar_wait(smem_u32(&full_bar[s]), ph, abort_flag)))
             break;
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t st = smem0 + s * C::kStageBytes;
           if (sti < st_base) {   // base GEMM: K blocks of 64 (4 MMAs of K=16 each)
             const uint64_t ad0 = make_smem_desc(st + C::a_off(0), 1024u, 2u);
             const uint64_t bd0 = make_smem_desc(st + C::b_off(0), 1024u, 2u);
@@ -473,10 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t swz = static_cast<uint32_t>(p.lora_swz);
             const uint32_t sbo = static_cast<uint32_t>(8 * lw * 2);
             const int nsub = min(cps, nl - (sti - st_base) * cps);
+            const uint64_t ad0 = make_smem_desc(st + C::lora_a_off(0, lw), sbo, swz);
+            const uint64_t bd0 = make_smem_desc(st + C::lora_b_off(0, lw), sbo, swz);
             for (int j = 0; j < nsub; ++j) {
               for (int kk = 0; kk < lw / 16; ++kk) {
-                const uint64_t ad = make_smem_desc(st + C::lora_a_off(j, lw) + kk * 32, sbo, swz);
-                const uint64_t bd = make_smem_desc(st + C::lora_b_off(j, lw) + kk * 32, sbo, swz);
+                const uint64_t ad = ad0 + static_cast<uint64_t>((C::lora_a_off(j, lw) + kk * 32) >> 4);
+                const uint64_t bd =
+                    bd0 + static_cast<uint64_t>((C::lora_b_off(j, lw) - C::lora_b_off(0, lw) + kk * 32) >> 4);
                 if (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, acc); else mma_bf16(d_tmem, ad, bd, idesc, acc);
                 acc = 1;
               }
@@ -484,6 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           issued = true;
           if (PAIR) mma_commit_pair(smem_u32(&empty_bar[s])); else mma_commit(smem_u32(&empty_bar[s]));
+          if (++sidx == C::kStages) {
+            sidx = 0;
+            sph ^= 1;
+          }
         }
         if (ok) {
           if (PAIR) mma_commit_pair(smem_u32(&accf_bar[buf])); else mma_commit(smem_u32(&accf_bar[buf]));
