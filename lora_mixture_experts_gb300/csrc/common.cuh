@@ -269,7 +269,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 // SiLU(v) = v * sigmoid(v) = v / (1 + e^-v), as v times the correctly rounded
 // reciprocal (for very negative v the reciprocal of +inf is 0, giving -0).
-__device__ __forceinline__ float silu_f(float v) { return v * __frcp_rn(1.0f + __expf(-v)); }
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // 32 lanes x 32 bit, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {

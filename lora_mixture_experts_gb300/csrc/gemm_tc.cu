@@ -60,7 +60,6 @@ struct RingEntry {
   TileInfo ti;
 };
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
-constexpr int kXchgStride = 17;          // floats per row of a gate/up exchange buffer
 
 template <int TN, bool PAIR>
 struct Cfg {
@@ -71,8 +70,7 @@ struct Cfg {
   static constexpr int kStages =
       PAIR ? 3 : (TN <= 16 ? 3 : (TN <= 32 ? 5 : (TN <= 64 ? 4 : (TN <= 128 ? 6 : 4))));
   static constexpr int kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;
-  static constexpr int kXchgBytes = 2 * 64 * kXchgStride * 4;   // gate and up halves
-  static constexpr int kBarOff = kStages * kStageBytes + kXchgBytes;
+  static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5 + 3 * kQ;
   static constexpr int kRingOff = kBarOff + kNumBars * 8 + 16;   // RingEntry[kQ]
   static constexpr int kSmemBytes = 1024 + kRingOff + kQ * static_cast<int>(sizeof(RingEntry));
@@ -170,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + C::kStages;
@@ -350,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nkb; ++j) {
               const int i = i0 + j;
               const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
-              if (gate_up)   // gate rows and the matching up rows in one box
-                load4(st + C::a_off(j), &maps.w, fb, kc * 64, grow, 0, ti.expert);
+              if (gate_up)   // 64 features, each gate row followed by its up row, in one box
+                load4(st + C::a_off(j), &maps.w, fb, kc * 64, 0, grow, ti.expert);
               else
                 load3(st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
               load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
@@ -386,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c = (i0 + j) - sl * p.lora_chunks;
                 const int a = p.slot_adapter[ti.slot_base + sl];
                 if (gate_up)
-                  load5(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, 0, ti.expert, a);
+                  load5(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, 0, grow, ti.expert, a);
                 else
                   load4(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, ti.expert, a);
                 load2(st + C::lora_b_off(j, lw), tz, fb, c * lw,
@@ -618,34 +615,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicAdd(&p.tile_done[it.tile], 1);
         }
       } else if (gate_up) {
-        // TMEM lanes 0-63 hold the gate rows and 64-127 the up rows of the
-        // same 64 features.  Per chunk of W columns the gate warps finish the
-        // first W/2 columns and the up warps the last W/2, each after taking
-        // the other half's values from a small shared-memory exchange.
-        const bool is_gate = row < 64;
-        const int f = row & 63;
-        const int feat = it.m * (PAIR ? 128 : 64) + static_cast<int>(rank) * 64 + f;
-        float* xg = xchg;                          // gate values of the up warps' columns
-        float* xu = xchg + 64 * kXchgStride;       // up values of the gate warps' columns
+        // TMEM lane 2i holds gate row i and lane 2i+1 the up row of the same
+        // feature (the weight box interleaves them), so a feature's two
+        // accumulator rows sit in adjacent threads of one warp.  Per chunk of
+        // W columns the gate thread finishes the first W/2 columns and the up
+        // thread the last W/2, each taking the values it lacks from its
+        // partner by one lane shuffle.
+        const bool is_gate = (row & 1) == 0;
+        const int feat = it.m * (PAIR ? 128 : 64) + static_cast<int>(rank) * 64 + (row >> 1);
         __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0) * p.out_ld + feat;
         const bool store_ok = feat < p.out_feats;
         auto finish = [&](const float* v, int c0, int half) {
           // v: this thread's W = 2*half values of columns c0 .. c0+W-1
-          if (is_gate) {
-            for (int cc = 0; cc < half; ++cc) xg[f * kXchgStride + cc] = v[half + cc];
-          } else {
-            for (int cc = 0; cc < half; ++cc) xu[f * kXchgStride + cc] = v[cc];
-          }
-          named_bar_sync(1, 128);
           const int cbase = c0 + (is_gate ? 0 : half);
+#pragma unroll
           for (int cc = 0; cc < half; ++cc) {
+            // the gate thread hands over its gate values of the up thread's
+            // columns, the up thread its up values of the gate thread's
+            const float other = __shfl_xor_sync(0xffffffffu, is_gate ? v[half + cc] : v[cc], 1);
+            const float g = is_gate ? v[cc] : other;
+            const float u = is_gate ? other : v[half + cc];
             const int c = cbase + cc;
-            const float g = is_gate ? v[cc] : xg[f * kXchgStride + cc];
-            const float u = is_gate ? xu[f * kXchgStride + cc] : v[half + cc];
             if (store_ok && c < ti.nrows)
               orow[static_cast<size_t>(c) * p.out_ld] = __float2bfloat16_rn(silu_f(g) * u);
           }
-          named_bar_sync(1, 128);
         };
         int c0 = 0;
         for (; c0 + 32 <= nmma; c0 += 32) {

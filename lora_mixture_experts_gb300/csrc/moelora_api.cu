@@ -403,21 +403,24 @@ bool enc3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
   return encode_map(m, base, 3, dims, str, box);
 }
 
-// gate_up weight [E][2I][K] seen as (K, I, 2, E): one box brings the gate
-// rows and the matching up rows of a 64-feature block.
+// gate_up weight [E][2I][K] seen as (K, 2, I, E): one box brings 64
+// features with each gate row followed by its up row (box row 2i = gate row
+// i, 2i + 1 = up row i), so that the two accumulator rows of a feature land
+// in adjacent TMEM lanes.
 bool enc_gate_up(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint64_t E) {
-  const uint64_t dims[4] = {K, I, 2, E};
-  const uint64_t str[3] = {K, I * K, 2 * I * K};
-  const uint32_t box[4] = {64, 64, 2, 1};
+  const uint64_t dims[4] = {K, 2, I, E};
+  const uint64_t str[3] = {I * K, K, 2 * I * K};
+  const uint32_t box[4] = {64, 2, 64, 1};
   return encode_map(m, base, 4, dims, str, box);
 }
 
-// gate_up LoRA expand weight [L][E][2I][r] seen as (r, I, 2, E, L).
+// gate_up LoRA expand weight [L][E][2I][r] seen as (r, 2, I, E, L), rows
+// interleaved like the weight's.
 bool enc_gate_up_lora(CUtensorMap* m, const void* base, uint64_t r, uint64_t I, uint64_t E,
                       uint64_t L, uint32_t box_w) {
-  const uint64_t dims[5] = {r, I, 2, E, L};
-  const uint64_t str[4] = {r, I * r, 2 * I * r, 2 * I * r * E};
-  const uint32_t box[5] = {box_w, 64, 2, 1, 1};
+  const uint64_t dims[5] = {r, 2, I, E, L};
+  const uint64_t str[4] = {I * r, r, 2 * I * r, 2 * I * r * E};
+  const uint32_t box[5] = {box_w, 2, 64, 1, 1};
   return encode_map(m, base, 5, dims, str, box);
 }
 
