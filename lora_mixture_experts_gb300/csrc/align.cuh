@@ -51,6 +51,9 @@ struct AlignArgs {
   ShrinkItem* shrink;
   int* slot_adapter;
   int* tile_done;
+  // 1: the single-CTA align zeroes the workspace error word before anything
+  // can flag it (the call then needs no separate memset)
+  int reset_err;
 };
 
 // The three align kernels; hist and scatter are skipped (return success)

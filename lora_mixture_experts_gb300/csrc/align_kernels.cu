@@ -316,6 +316,10 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
   grid_dependency_wait();
   grid_dependency_trigger();
   const int tid = threadIdx.x;
+  if (a.reset_err) {   // the call's first kernel clears the error word itself
+    if (tid == 0) a.hdr->err = 0;
+    __syncthreads();
+  }
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int f = tid;
@@ -442,16 +446,25 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
                                                       const int* __restrict__ pos_of,
                                                       uint2* __restrict__ out, int T, int kk,
                                                       int nsplit, int hv, long long split_stride4) {
-  grid_dependency_wait();
-  grid_dependency_trigger();
   const int k = K > 0 ? K : kk;
   const int ns = NS > 0 ? NS : nsplit;
   const int lane = threadIdx.x & 31;
   const int per_tok = (hv + 32 * kCombUnroll - 1) / (32 * kCombUnroll);
   const long long items = static_cast<long long>(T) * per_tok;
   const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); w < items;
-       w += nw) {
+  const long long w0 = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5);
+  // the rows of the warp's first token come from the align, which completed
+  // before the preceding launch let this one start: read them before waiting
+  // for the partial rows themselves
+  int pos0[K > 0 ? K : 1];
+  if (K > 0 && w0 < items) {
+    const int t0 = static_cast<int>(w0 / per_tok);
+#pragma unroll
+    for (int j = 0; j < (K > 0 ? K : 1); ++j) pos0[j] = pos_of[static_cast<size_t>(t0) * K + j];
+  }
+  grid_dependency_wait();
+  grid_dependency_trigger();
+  for (long long w = w0; w < items; w += nw) {
     const int t = static_cast<int>(w / per_tok);
     const int c0 = static_cast<int>(w - static_cast<long long>(t) * per_tok) * 32 * kCombUnroll + lane;
     float4 acc[kCombUnroll];
@@ -460,7 +473,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
     if (K > 0 && NS > 0) {
       int pos[K > 0 ? K : 1];
 #pragma unroll
-      for (int j = 0; j < K; ++j) pos[j] = pos_of[static_cast<size_t>(t) * K + j];
+      for (int j = 0; j < K; ++j) pos[j] = w == w0 ? pos0[j] : pos_of[static_cast<size_t>(t) * K + j];
       float4 v[K > 0 ? K : 1][NS > 0 ? NS : 1][kCombUnroll];
 #pragma unroll
       for (int j = 0; j < K; ++j)

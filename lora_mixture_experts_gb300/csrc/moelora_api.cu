@@ -476,14 +476,16 @@ struct Launcher {
   }
 };
 
-// The align kernels (one kernel for small batches); the first follows a
-// memset and is not chained.
-cudaError_t run_align(Launcher& ln, const AlignArgs& a, cudaStream_t stream) {
+// The align kernels (one kernel for small batches, which also clears the
+// workspace error word; otherwise a memset does), the first not chained.
+cudaError_t run_align(Launcher& ln, AlignArgs a, cudaStream_t stream) {
   cudaError_t e;
   if (a.n > 0 && align_small_fits(a)) {
+    a.reset_err = 1;
     ln.before("align_small");
     return launch_align_small(a, stream, false);
   }
+  if ((e = cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream)) != cudaSuccess) return e;
   bool first = true;
   if (a.logits) {
     ln.before("route");
@@ -653,7 +655,6 @@ int moe_lora_align(const moelora_dims* d, const int32_t* topk_ids, const int32_t
   a.seg_off = seg_off;
   a.num_post_pad = num_post_pad;
   Launcher ln(stream);
-  MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
   MOELORA_CUDA_CHECK(run_align(ln, a, stream));
   ln.finish();
   return MOELORA_OK;
@@ -769,7 +770,6 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.work_ctr = &a.hdr->work[1];
 
   Launcher ln(stream);
-  MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
   MOELORA_CUDA_CHECK(run_align(ln, a, stream));
   ln.before("permute");
   MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
@@ -889,7 +889,6 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   }
 
   Launcher ln(stream);
-  MOELORA_CUDA_CHECK(cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream));
   MOELORA_CUDA_CHECK(run_align(ln, a, stream));
   ln.before("permute");
   MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
