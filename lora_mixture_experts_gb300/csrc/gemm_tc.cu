@@ -221,14 +221,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
   }
-  // results of the preceding launch (x_perm / act, the tile tables) are read
-  // only after this point; the next launch may start its own preamble
-  grid_dependency_wait();
-  grid_dependency_trigger();
   tc_fence_before();
   __syncthreads();
   if (PAIR) cluster_sync();   // the peer's barriers exist before any remote signal
   tc_fence_after();
+  // Results of the preceding launch (x_perm / act) are read only after the
+  // grid dependency wait; the next launch may start its own preamble.  On
+  // unpaired tiles the scheduling and producer warps do not wait here: the
+  // tile tables and item counters come from the align, which had completed
+  // before the preceding launch let this one start, and the weights are
+  // inputs, so the producer streams the weight blocks of its first stages
+  // while the preceding kernel drains and waits before the first token rows.
+  const bool early = !PAIR && p.early_weights && (warp == 0 || warp == kSchedWarp);
+  if (!early) grid_dependency_wait();
+  grid_dependency_trigger();
   const uint32_t tmem_base = *tmem_holder;
 
   const int n_tiles = p.hdr->n_tiles;
@@ -272,6 +278,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load5 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z, int w,
                        int v) {
         if (PAIR) tma_load_5d_pair(dst, m, fb, x, y, z, w, v); else tma_load_5d(dst, m, fb, x, y, z, w, v);
+      };
+      // Before the grid dependency wait (first item only, unpaired tiles),
+      // a stage gets its weight blocks and its barrier's byte count; the
+      // token rows of those stages (slots 0 .. n_def-1, K chunk i of the item
+      // = kc0 + i rotated by rot within nkc) are loaded after the wait, which
+      // comes once the ring is full or the item's K loop ends.
+      bool waited = !early;
+      int n_def = 0;
+      auto load_deferred_rows = [&](int nkc, int kc0, int rot, const CUtensorMap* tb, int brow0) {
+        grid_dependency_wait();
+        for (int d = 0; d < n_def; ++d) {
+          const uint32_t st = smem_u32(smem + d * C::kStageBytes);
+          const uint32_t fb = smem_u32(&full_bar[d]);
+          for (int j = 0; j < C::kKB && d * C::kKB + j < nkc; ++j) {
+            const int i = d * C::kKB + j;
+            const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
+            load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+          }
+        }
+        waited = true;
       };
       // stage s of this CTA is free: wait on its empty barrier; the barrier
       // that counts the stage's bytes is the leader's full barrier
@@ -323,9 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int q = 0; q < ns_me; ++q)
                 load4(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
                       p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
-              load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+              if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
+            if (!waited && ++n_def == C::kStages) load_deferred_rows(nk, 0, 0, tb, brow0);
           }
+          if (!waited) load_deferred_rows(nk, 0, 0, tb, brow0);
         } else {
           const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
           const int kc0 = it.ks * nks;
@@ -351,9 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load4(st + C::a_off(j), &maps.w, fb, kc * 64, 0, grow, ti.expert);
               else
                 load3(st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
-              load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+              if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
+            if (!waited && ++n_def == C::kStages) load_deferred_rows(nkc, kc0, rot, tb, brow0);
           }
+          if (!waited) load_deferred_rows(nkc, kc0, rot, tb, brow0);
           if (ok && p.r > 0 && ti.nslots > 0 && it.ks == p.ksplit - 1) {
             // the tile's shrink results must be complete and visible to TMA
             const int target = p.done_target * ti.nsh * done_scale;

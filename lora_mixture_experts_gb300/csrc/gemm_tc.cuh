@@ -46,6 +46,8 @@ struct GemmParams {
   float* out_f32;       // y_pair [Pmax][H] (down): gate-weighted expert output, fp32
   int out_ld;
   int* work_ctr;        // items claimed so far (zeroed by the align); NULL = fixed shares
+  int early_weights;    // 1: on unpaired tiles, stream the first weight blocks before
+                        //    the preceding launch has finished (see the kernel)
 };
 
 // Launches one GEMM phase (shrink items first, then the main items) as a

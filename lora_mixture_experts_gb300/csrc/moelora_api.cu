@@ -768,6 +768,10 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.split_stride = static_cast<long long>(p.Pmax) * p.H;
   gd.out_ld = p.H;
   gd.work_ctr = &a.hdr->work[1];
+  // the down phase's weights stream while the gate_up launch drains (measured:
+  // decode 249.0 -> 246.4 us; on the gate_up and dense-linear launches, whose
+  // predecessor is the short permute, the deferred first token rows cost more)
+  gd.early_weights = 1;
 
   Launcher ln(stream);
   MOELORA_CUDA_CHECK(run_align(ln, a, stream));
