@@ -477,13 +477,16 @@ struct Launcher {
 };
 
 // The align kernels (one kernel for small batches, which also clears the
-// workspace error word; otherwise a memset does), the first not chained.
+// workspace error word; otherwise a memset does).  The single-CTA align is
+// chained to whatever precedes it on the stream: it waits for that kernel's
+// completion before its first read or write (a preceding call's combine may
+// still be reading this workspace), so only its launch overlaps.
 cudaError_t run_align(Launcher& ln, AlignArgs a, cudaStream_t stream) {
   cudaError_t e;
   if (a.n > 0 && align_small_fits(a)) {
     a.reset_err = 1;
     ln.before("align_small");
-    return launch_align_small(a, stream, false);
+    return launch_align_small(a, stream, true);
   }
   if ((e = cudaMemsetAsync(&a.hdr->err, 0, sizeof(int), stream)) != cudaSuccess) return e;
   bool first = true;
