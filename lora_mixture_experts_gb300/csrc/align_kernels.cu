@@ -600,6 +600,9 @@ cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16
     if (k == 4) return go(combine_kernel<4, 2>);
     if (k == 6) return go(combine_kernel<6, 2>);
     if (k == 8) return go(combine_kernel<8, 2>);
+  } else if (k == 1) {   // the dense linear's finer K splits
+    if (nsplit == 3) return go(combine_kernel<1, 3>);
+    if (nsplit == 4) return go(combine_kernel<1, 4>);
   }
   return go(combine_kernel<0, 0>);
 }

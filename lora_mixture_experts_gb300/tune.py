@@ -23,7 +23,7 @@ from .inputs import CONFIGS, LinearCase, make_linear_case, make_moe_case
 TILES = (16, 32, 64, 128, 256)
 
 
-def _time(fn, warmup=5, iters=30):
+def _time(fn, warmup=5, iters=100):
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -80,7 +80,7 @@ def sweep(names, out_path, device="cuda", log=print):
             default_ms = _time(make())
             best = None
             for tn in TILES:
-                for ks in ((1, 2, 4) if rows <= 64 else (1,)):
+                for ks in ((1, 2, 3, 4) if rows <= 64 else (1,)):
                     with open(cand_file, "w") as f:
                         f.write(f"{_shape_line(case)} tn={tn} ksplit={ks}\n")
                     binding.moelora_load_tuning(cand_file)

@@ -129,7 +129,7 @@ def test_forward_prefill_sampled():
 @pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
 def test_forward_skewed_sampled(tuned):
     # the tuned table (the launch configuration bench.py times) runs this
-    # workload on paired 256-token tiles with a split down phase
+    # workload on larger token tiles than the built-in choice
     import os
     table = os.path.join(os.path.dirname(binding.__file__), "tuning")
     binding.moelora_load_tuning(table if tuned else None)
@@ -232,12 +232,21 @@ def test_forward_bad_index_flag():
 
 
 # ------------------------------------------------------------------ dense linear
+@pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
 @pytest.mark.parametrize("T", DENSE_T_SWEEP)
-def test_linear_dense(T):
+def test_linear_dense(T, tuned):
+    # the tuned table is the launch configuration bench.py times (its token
+    # tile and K split differ from the built-in choice for some T)
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
     c = CONFIGS[f"dense_t{T}"]
     d = make_linear_case(c, seed=0, device=DEV)
-    out = binding.moe_lora_linear(d["x"], d["lora_ids"], d["W"], d["A"], d["B"])
-    torch.cuda.synchronize()
+    binding.moelora_load_tuning(table if tuned else None)
+    try:
+        out = binding.moe_lora_linear(d["x"], d["lora_ids"], d["W"], d["A"], d["B"])
+        torch.cuda.synchronize()
+    finally:
+        binding.moelora_load_tuning(None)
     tokens = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(2).choice(T, 16, replace=False))
     x = np_inputs({"x": d["x"]})["x"][tokens]
     lo = d["lora_ids"].cpu().numpy()[tokens]
