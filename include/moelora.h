@@ -44,7 +44,7 @@ typedef struct CUstream_st* moelora_stream_t;   /* == cudaStream_t */
 enum {
   MOELORA_OK = 0,
   MOELORA_ERR_INVALID_ARG = -1,   /* null pointer, negative size, k > E ... */
-  MOELORA_ERR_UNSUPPORTED = -2,   /* H, I not multiples of 8; r not in {16,32,64,128} */
+  MOELORA_ERR_UNSUPPORTED = -2,   /* H, I not multiples of 8; r not a multiple of 16 in 16..128 */
   MOELORA_ERR_MISALIGNED = -3,    /* a bf16 pointer not 16-byte aligned */
   MOELORA_ERR_WORKSPACE = -4,     /* workspace null or smaller than required */
   MOELORA_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */

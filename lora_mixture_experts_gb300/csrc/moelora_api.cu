@@ -160,7 +160,13 @@ void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, i
   }
 }
 
-bool lora_rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
+// LoRA ranks: multiples of 16 (the MMA's K step) up to 128 (one adapter's
+// rows fill a 128-row shrink tile).
+bool lora_rank_ok(int r) { return r >= 16 && r <= 128 && r % 16 == 0; }
+
+// Width of one LoRA K chunk in shared memory: the largest of 64, 32, 16
+// elements that divides r (a swizzle atom row of 128, 64 or 32 bytes).
+uint32_t lora_chunk_width(int r) { return r % 64 == 0 ? 64u : (r % 32 == 0 ? 32u : 16u); }
 
 int check_moe_dims(const moelora_dims* d) {
   if (!d) return MOELORA_ERR_INVALID_ARG;
@@ -565,7 +571,8 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
   // not the long pole -- with 8 adapters of r=16 over K=8192 one stacked
   // item streamed 2 MB while every main item streamed 1 MB.
   const bool paired = moe_gemm_paired(p.tn);
-  a.spi = p.lora ? (paired ? 256 / p.r : std::max(1, 128 / (p.r * p.ksplit))) : 0;
+  // slots per shrink item: whole adapters per 128-row tile, on each CTA of a pair
+  a.spi = p.lora ? (paired ? 2 * (128 / p.r) : std::max(1, 128 / (p.r * p.ksplit))) : 0;
   a.tiles = ws_ptr<TileInfo>(ws, p.off_tiles);
   a.shrink = ws_ptr<ShrinkItem>(ws, p.off_shrink);
   a.slot_adapter = ws_ptr<int>(ws, p.off_slot_ad);
@@ -578,7 +585,7 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   g.ksplit = 1;
   g.split_stride = 0;
   g.r = p.r;
-  g.lora_w = p.lora ? std::min(p.r, 64) : 64;
+  g.lora_w = p.lora ? static_cast<int>(lora_chunk_width(p.r)) : 64;
   g.lora_chunks = p.lora ? p.r / g.lora_w : 0;
   g.lora_swz = g.lora_w >= 64 ? 2 : (g.lora_w >= 32 ? 4 : 6);
   g.slots_per_item = p.lora ? 128 / p.r : 0;
@@ -716,7 +723,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   auto* act = ws_ptr<__nv_bfloat16>(ws, p.off_act);
   auto* ypair = ws_ptr<float>(ws, p.off_ypair);
   const uint64_t zrows = static_cast<uint64_t>(std::max(p.n_slots_max, 1)) * p.tn;
-  const uint32_t lw = p.lora ? std::min(p.r, 64) : 64;
+  const uint32_t lw = p.lora ? lora_chunk_width(p.r) : 64u;
 
   // gate_up phase maps
   GemmMaps mg;
@@ -860,7 +867,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   auto* x_perm = ws_ptr<__nv_bfloat16>(ws, p.off_xperm);
   auto* z = ws_ptr<__nv_bfloat16>(ws, p.off_zgu);
   const uint64_t zrows = static_cast<uint64_t>(std::max(p.n_slots_max, 1)) * p.tn;
-  const uint32_t lw = p.lora ? std::min(p.r, 64) : 64;
+  const uint32_t lw = p.lora ? lora_chunk_width(p.r) : 64u;
 
   GemmMaps m;
   std::memset(&m, 0, sizeof(m));

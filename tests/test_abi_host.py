@@ -69,6 +69,8 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, _d(k=33)) == INVALID
     assert _fwd(lib, _d(I=2884)) == UNSUP
     assert _fwd(lib, _d(r=8)) == UNSUP
+    assert _fwd(lib, _d(r=40)) == UNSUP
+    assert _fwd(lib, _d(r=144)) == UNSUP
     assert _fwd(lib, _d(E=2048, k=2)) == UNSUP
     p = [ctypes.c_void_p(FAKE)] * 11
     p[0] = None                                              # x

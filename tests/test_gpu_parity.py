@@ -154,6 +154,11 @@ SMALL = [
     (8, 136, 2048, 4, 2, 2, 16),     # few rows per expert, long K: the down phase splits K
     (600, 256, 200, 2, 1, 3, 32),    # 256-row tiles on CTA pairs, partial tiles and feature blocks
     (520, 136, 72, 2, 2, 2, 128),    # CTA pairs, rank 128: one adapter per CTA in a shrink item
+    (37, 200, 264, 5, 2, 3, 48),     # rank 48: 16-wide expand chunks, two adapters per shrink tile
+    (530, 136, 200, 2, 2, 3, 48),    # CTA pairs at rank 48: two adapters on each CTA of an item
+    (23, 264, 136, 4, 3, 2, 96),     # rank 96: 32-wide chunks, one adapter per shrink tile
+    (300, 128, 256, 2, 1, 3, 80),    # CTA pairs at rank 80
+    (45, 256, 128, 3, 2, 2, 112),    # rank 112
 ]
 
 
@@ -260,7 +265,8 @@ def test_linear_dense(T, tuned):
 
 def test_linear_small_no_lora_and_ragged():
     g = torch.Generator(device=DEV).manual_seed(4)
-    for (T, K, N, L, r) in [(3, 64, 136, 0, 0), (45, 200, 264, 3, 32), (260, 128, 128, 2, 64)]:
+    for (T, K, N, L, r) in [(3, 64, 136, 0, 0), (45, 200, 264, 3, 32), (260, 128, 128, 2, 64),
+                            (33, 192, 264, 3, 48), (270, 136, 128, 2, 96)]:
         x = torch.randn(T, K, generator=g, device=DEV).bfloat16()
         W = (torch.randn(N, K, generator=g, device=DEV) * K ** -0.5).bfloat16()
         A = (torch.randn(L, r, K, generator=g, device=DEV) * K ** -0.5).bfloat16() if L else None
