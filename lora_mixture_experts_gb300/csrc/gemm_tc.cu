@@ -61,6 +61,7 @@ struct RingEntry {
 };
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
 
+
 template <int TN, bool PAIR>
 struct Cfg {
   static constexpr int kRowsB = PAIR ? TN / 2 : TN;   // token rows a CTA holds per K block
@@ -398,7 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_global();
             const CUtensorMap* tz = &maps.z[bi];
             const int lw = p.lora_w;
-            const int nl = ti.nslots * p.lora_chunks;   // expand chunks: (slot, chunk) pairs
+            // expand chunks: (slot, chunk, part), the part (hi, lo) fastest so
+            // that a LoRA B chunk is read twice in a row (the second from L2)
+            const int nl = ti.nslots * p.lora_chunks * p.z_parts;
             const uint32_t per_sub = (PAIR ? 2 : 1) * (128 * lw * 2 + brows * lw * 2);
             const int cps = C::kKB * 64 / lw;           // chunks packed per stage
             for (int i0 = 0; i0 < nl && ok; i0 += cps, advance()) {
@@ -409,14 +412,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t st = smem_u32(smem + s * C::kStageBytes);
               if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nsub * per_sub);
               for (int j = 0; j < nsub; ++j) {
-                const int sl = (i0 + j) / p.lora_chunks;
-                const int c = (i0 + j) - sl * p.lora_chunks;
+                const int per_slot = p.lora_chunks * p.z_parts;
+                const int sl = (i0 + j) / per_slot;
+                const int cp = (i0 + j) - sl * per_slot;
+                const int c = cp / p.z_parts;
+                const int part = cp - c * p.z_parts;
                 const int a = p.slot_adapter[ti.slot_base + sl];
                 if (gate_up)
                   load5(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, 0, grow, ti.expert, a);
                 else
                   load4(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, ti.expert, a);
-                load2(st + C::lora_b_off(j, lw), tz, fb, c * lw,
+                load2(st + C::lora_b_off(j, lw), tz, fb, part * p.r + c * lw,
                       (ti.slot_base + sl) * TN + static_cast<int>(rank) * nh);
               }
             }
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * TN;
         const int nl =
-            (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks : 0;
+            (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks * p.z_parts : 0;
         const int nb = it.shrink ? nk : min(nk, (it.ks + 1) * nks) - it.ks * nks;
         const int st_base = (nb + C::kKB - 1) / C::kKB;
         const int cps = p.r > 0 ? C::kKB * 64 / p.lora_w : 1;   // expand chunks per stage
@@ -624,7 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = row % p.r;
         const bool valid = j < si.nslot && row / p.r < spc;
         const int a_j = valid ? p.slot_adapter[si.slot0 + j] : -3;
-        __nv_bfloat16* zrow = p.zbuf + (static_cast<size_t>(si.slot0 + (valid ? j : 0)) * TN) * p.r + q;
+        __nv_bfloat16* zrow =
+            p.zbuf + (static_cast<size_t>(si.slot0 + (valid ? j : 0)) * TN) * (p.z_parts * p.r) + q;
         for (int c0 = 0; c0 < nmma; c0 += 16) {
           float v[16];
           tmem_ld16(t_row + c0, v);
@@ -633,7 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < 16; ++cc) {
               const int c = c0 + cc;
               const bool keep = c < ti.nrows && p.row_lora[ti.row0 + c] == a_j;
-              zrow[static_cast<size_t>(c) * p.r] = __float2bfloat16_rn(keep ? v[cc] : 0.0f);
+              const float z = keep ? v[cc] : 0.0f;
+              const __nv_bfloat16 hi = __float2bfloat16_rn(z);
+              zrow[static_cast<size_t>(c) * (p.z_parts * p.r)] = hi;
+              if (p.z_parts == 2)
+                zrow[static_cast<size_t>(c) * (2 * p.r) + p.r] = __float2bfloat16_rn(z - __bfloat162float(hi));
             }
           }
         }

@@ -41,7 +41,14 @@ struct GemmParams {
   const float* row_w;
   const int* row_tok;
   int* tile_done;
-  __nv_bfloat16* zbuf;  // [slots * tn][r]
+  // Shrink results [slots * tn][z_parts * r].  z_parts = 2 keeps each as two
+  // bf16 rows, hi = bf16(z) and lo = bf16(z - hi) ([hi r | lo r]), and the
+  // expand multiplies both, seeing z to about 16 significant bits: used for
+  // the gate_up LoRA, whose rounding error SiLU(gate) * up amplifies (a
+  // single bf16 z there put outputs 6-7 RMS from zero past 3e-2 x RMS).
+  // z_parts = 1: one bf16 row (down and dense linear).
+  __nv_bfloat16* zbuf;
+  int z_parts;
   __nv_bfloat16* out;   // act [Pmax][I] (gate_up) or out [T][N] (linear)
   float* out_f32;       // y_pair [Pmax][H] (down): gate-weighted expert output, fp32
   int out_ld;

@@ -232,7 +232,9 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   p.off_slot_ad = b.take(static_cast<size_t>(std::max(p.n_slots_max, 1)) * 4);
   p.off_tile_done = b.take(static_cast<size_t>(p.n_tiles_max) * 4);
   p.off_xperm = b.take(static_cast<size_t>(p.Pmax) * p.H * 2);
-  const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
+  // gate_up shrink results: per slot and token row, hi and lo bf16 rows of r
+  // (the dense linear uses the first half only)
+  const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2 * 2;
   p.off_zgu = b.take(std::max<size_t>(zbytes, 16));
 }
 
@@ -281,7 +283,7 @@ Plan plan_forward(const moelora_dims* d) {
   Bump b;
   plan_align_scratch(p, b);
   plan_gemm_tables(p, b);
-  const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;
+  const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2;   // one bf16 row
   p.off_zd = b.take(std::max<size_t>(zbytes, 16));
   p.off_act = b.take(static_cast<size_t>(p.Pmax) * p.I * 2);
   p.off_topk_ids = b.take(static_cast<size_t>(p.n) * 4);
@@ -589,6 +591,7 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   g.lora_chunks = p.lora ? p.r / g.lora_w : 0;
   g.lora_swz = g.lora_w >= 64 ? 2 : (g.lora_w >= 32 ? 4 : 6);
   g.slots_per_item = p.lora ? 128 / p.r : 0;
+  g.z_parts = 1;
   g.hdr = a.hdr;
   g.err = &a.hdr->err;
   g.tiles = a.tiles;
@@ -733,7 +736,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   if (p.lora) {
     ok = ok && enc_gate_up_lora(&mg.lb, B_gu, p.r, p.I, p.E, p.L, lw);
     ok = ok && enc4(&mg.la, A_gu, p.H, p.r, p.E, p.L, 64, p.r);
-    ok = ok && enc_row_maps(mg.z, zgu, p.r, zrows, lw, p.tn);
+    ok = ok && enc_row_maps(mg.z, zgu, 2 * p.r, zrows, lw, p.tn);
   }
   // down phase maps
   GemmMaps md;
@@ -759,6 +762,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   const double rows_per_expert = static_cast<double>(p.n) / p.E;
   gu.group_tiles = group_tiles(p.tn, gu.n_mtiles, rows_per_expert, units);
   gu.zbuf = zgu;
+  gu.z_parts = 2;   // the gate_up shrink result as a bf16 hi/lo pair
   gu.out = act;
   gu.out_ld = p.I;
   gu.work_ctr = &a.hdr->work[0];

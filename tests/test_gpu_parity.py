@@ -174,6 +174,35 @@ def test_forward_small_shapes(shape):
     _run_parity(d, what=str(shape))
 
 
+def _random_shapes(n, seed):
+    """Seeded random small layer shapes: sizes off the tile grid, any rank the
+    library takes, both routings and adapter mixes, with or without LoRA."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        E = int(rng.integers(1, 17))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        L = int(rng.integers(0, 6))
+        out.append(dict(T=int(rng.integers(1, 301)), H=8 * int(rng.integers(8, 41)),
+                        I=8 * int(rng.integers(8, 41)), E=E, k=k, L=L,
+                        r=16 * int(rng.integers(1, 9)) if L else 0,
+                        routing=str(rng.choice(["uniform", "zipf"])),
+                        adapters=str(rng.choice(["uniform_with_none", "zipf"]))))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_shapes(24, 17), ids=lambda s: "T{T}_H{H}_I{I}_E{E}_k{k}_L{L}_r{r}".format(**s))
+def test_forward_random_shapes(shape):
+    s = shape
+    L, r = (s["L"], s["r"]) if s["L"] else (1, 16)
+    c = small_moe_case(s["T"], s["H"], s["I"], s["E"], s["k"], L, r, adapters=s["adapters"],
+                       routing=s["routing"])
+    d = make_moe_case(c, seed=23, device=DEV, lora=s["L"] > 0)
+    if s["L"] == 0:
+        d["lora_ids"] = torch.full((s["T"],), -1, dtype=torch.int32, device=DEV)
+    _run_parity(d, what=str(s))
+
+
 def test_forward_many_experts_top8():
     c = small_moe_case(1024, 128, 192, 64, 8, 4, 16, adapters="zipf", routing="zipf")
     d = make_moe_case(c, seed=6, device=DEV)
@@ -260,6 +289,27 @@ def test_linear_dense(T, tuned):
     B = np_inputs({"B": d["B"]})["B"]
     exp = ref.moe_lora_linear_ref(x, lo, W, A, B)
     ok, msg = compare(out[torch.as_tensor(tokens, device=DEV)], exp, f"dense T={T}")
+    assert ok, msg
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_linear_random_shapes(seed):
+    # seeded random dense multi-LoRA linears: ragged T, K and N off the tile
+    # grid, any rank the library takes, some tokens without an adapter
+    rng = np.random.default_rng(100 + seed)
+    T, K, N = int(rng.integers(1, 600)), 8 * int(rng.integers(8, 80)), 8 * int(rng.integers(8, 80))
+    L = int(rng.integers(0, 9))
+    r = 16 * int(rng.integers(1, 9)) if L else 0
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn(T, K, generator=g, device=DEV).bfloat16()
+    W = (torch.randn(N, K, generator=g, device=DEV) * K ** -0.5).bfloat16()
+    A = (torch.randn(L, r, K, generator=g, device=DEV) * K ** -0.5).bfloat16() if L else None
+    B = (torch.randn(L, N, r, generator=g, device=DEV) * r ** -0.5).bfloat16() if L else None
+    lo = (torch.randint(-1, L, (T,), generator=g, device=DEV) if L else torch.full((T,), -1, device=DEV)).int()
+    out = binding.moe_lora_linear(x, lo, W, A, B)
+    n = np_inputs({"x": x, "W": W, **({"A": A, "B": B} if L else {})})
+    exp = ref.moe_lora_linear_ref(n["x"], lo.cpu().numpy(), n["W"], n.get("A"), n.get("B"))
+    ok, msg = compare(out, exp, f"linear T={T} K={K} N={N} L={L} r={r}")
     assert ok, msg
 
 
