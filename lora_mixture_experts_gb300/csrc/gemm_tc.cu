@@ -242,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_sh = p.r > 0 ? p.hdr->n_shrink : 0;
   const int n_items = n_sh + n_tiles * p.n_mtiles * p.ksplit;
   const int nk = (p.K + 63) / 64;             // 64-wide K chunks of the base GEMM
-  const int nks = (nk + p.ksplit - 1) / p.ksplit;   // chunks per K split
   const bool gate_up = p.mode == kModeGateUp;
   const int spc = p.r > 0 ? 128 / p.r : 0;    // shrink slots per CTA
   // shrink completions a tile's item waits for: every CTA of the item signals
@@ -357,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!waited) load_deferred_rows(nk, 0, 0, tb, brow0);
         } else {
           const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
-          const int kc0 = it.ks * nks;
-          const int nkc = min(nk, kc0 + nks) - kc0;
+          const int kc0 = p.split_k0[it.ks];
+          const int nkc = p.split_k0[it.ks + 1] - kc0;
           // (paired tiles, tensor-bound: the token tiles of one expert read
           // the same weight blocks at the same time, so no rotation there)
           const int rot = PAIR ? 0 : k_rotation(it, nkc);
@@ -470,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + buf * TN;
         const int nl =
             (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks * p.z_parts : 0;
-        const int nb = it.shrink ? nk : min(nk, (it.ks + 1) * nks) - it.ks * nks;
+        const int nb = it.shrink ? nk : p.split_k0[it.ks + 1] - p.split_k0[it.ks];
         const int st_base = (nb + C::kKB - 1) / C::kKB;
         const int cps = p.r > 0 ? C::kKB * 64 / p.lora_w : 1;   // expand chunks per stage
         const int st_all = st_base + (nl + cps - 1) / cps;

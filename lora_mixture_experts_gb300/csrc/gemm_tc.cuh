@@ -17,6 +17,8 @@ struct alignas(64) GemmMaps {
   CUtensorMap z[5];   // shrink results, 2D (r, slots * tn)
 };
 
+constexpr int kMaxKSplit = 4;
+
 struct GemmParams {
   int mode;            // GemmMode
   int K;               // base reduction length
@@ -31,6 +33,9 @@ struct GemmParams {
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
   int group_tiles;     // token tiles per L2 group of the main-item order
   int ksplit;          // K splits of the main items (down mode: fp32 partial per split)
+  // first 64-wide K block of each split, split_k0[ksplit] = K blocks in all;
+  // the last split is the shortest (see split_starts on the host)
+  int split_k0[kMaxKSplit + 1];
   long long split_stride;  // elements between the fp32 partials of consecutive splits
   const WsHeader* hdr;
   int* err;
