@@ -24,12 +24,10 @@ struct GemmParams {
   int K;               // base reduction length
   int n_mtiles;        // weight tiles per token tile (128 rows; 256 on CTA pairs)
   int out_feats;       // valid output features (I, H or N)
-  int half_rows;       // gate_up: row offset of the `up` half (= I)
   int r;               // LoRA rank, 0 = no LoRA
   int lora_w;          // elements of one LoRA K-chunk in shared memory (<= 64)
   int lora_chunks;     // r / lora_w
   int lora_swz;        // descriptor layout code of a LoRA chunk
-  int slots_per_item;  // 128 / r
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
   int group_tiles;     // token tiles per L2 group of the main-item order
   int ksplit;          // K splits of the main items (down mode: fp32 partial per split)

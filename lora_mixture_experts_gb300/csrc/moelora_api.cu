@@ -615,7 +615,6 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   g.lora_w = p.lora ? static_cast<int>(lora_chunk_width(p.r)) : 64;
   g.lora_chunks = p.lora ? p.r / g.lora_w : 0;
   g.lora_swz = g.lora_w >= 64 ? 2 : (g.lora_w >= 32 ? 4 : 6);
-  g.slots_per_item = p.lora ? 128 / p.r : 0;
   g.z_parts = 1;
   g.hdr = a.hdr;
   g.err = &a.hdr->err;
@@ -782,7 +781,6 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   const bool paired = moe_gemm_paired(p.tn);
   gu.n_mtiles = (p.I + (paired ? 127 : 63)) / (paired ? 128 : 64);
   gu.out_feats = p.I;
-  gu.half_rows = p.I;
   gu.done_target = 1;
   const int units = paired ? sms / 2 : sms;
   const double rows_per_expert = static_cast<double>(p.n) / p.E;
@@ -798,7 +796,6 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.K = p.I;
   gd.n_mtiles = (p.H + (paired ? 255 : 127)) / (paired ? 256 : 128);
   gd.out_feats = p.H;
-  gd.half_rows = 0;
   gd.done_target = 2;
   gd.group_tiles = group_tiles(p.tn, gd.n_mtiles, rows_per_expert, units);
   gd.zbuf = zd;
