@@ -39,8 +39,8 @@ METRIC = "MoE-LoRA layer routed tokens/s; % of HBM (decode) / bf16 TC (prefill) 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
