@@ -54,6 +54,13 @@ struct AlignArgs {
   // 1: the single-CTA align zeroes the workspace error word before anything
   // can flag it (the call then needs no separate memset)
   int reset_err;
+  // Row gather fused into the small-batch align (no router): with x set, the
+  // kernel runs on several CTAs; each computes the order in its own shared
+  // memory, CTA 0 alone writes the tables, and the others copy the token
+  // rows, x_perm[row] = x[token of row] (hv 16-byte pieces per row).
+  const uint4* x;
+  uint4* x_perm;
+  int hv;
 };
 
 // The three align kernels; hist and scatter are skipped (return success)
@@ -70,10 +77,11 @@ constexpr int kRouteMaxE = 1024;
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                          cudaStream_t stream, bool chained);
 
-// The same align in one single-CTA kernel, for small batches.
+// The same align in one single-CTA kernel, for small batches; with a.x set
+// (and no router) it also gathers the token rows into x_perm on extra CTAs.
 constexpr int kSmallMaxBins = 8192;
 bool align_small_fits(const AlignArgs& a);
-cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained);
+cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained, int num_sms);
 
 // x_perm[p] = x[row_tok[p]] (zero rows for padding), p < Pmax.
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,

@@ -153,7 +153,9 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 // bin starts there (and copied to a.bin_start).  Reading the bins from shared
 // memory keeps the per-expert loops free of global round trips.  Run by all
 // threads of one CTA (at least one per expert).
-__device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
+// With write == false (the extra CTAs of the fused small align) only the bin
+// starts in sb are computed; nothing is written to global memory.
+__device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool write = true) {
   const int tid = threadIdx.x;
   const int Lp = a.L + 1;
   // one expert per thread
@@ -173,10 +175,15 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb) {
       const int b = e * Lp + l;
       const int tot = sb[b];
       sb[b] = s;
-      a.bin_start[b] = s;
-      if (a.seg_off) a.seg_off[b] = s;
+      if (write) {
+        a.bin_start[b] = s;
+        if (a.seg_off) a.seg_off[b] = s;
+      }
       s += tot;
     }
+  }
+  if (!write) return;
+  if (has_e) {
     for (int blk = start / a.block_m; blk < (start + pad) / a.block_m; ++blk) a.blk_expert[blk] = e;
     for (int p = start + cnt; p < start + pad; ++p) {
       a.sorted_ids[p] = a.n;
@@ -312,11 +319,15 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
 // tables step, then the scatter.  Same results as hist + scan + scatter.
 __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) {
   __shared__ int warp_sums[32];
-  extern __shared__ int sm_bins[];   // [nbins] running counts
+  extern __shared__ int sm_bins[];   // [nbins] running counts, then [n] positions (gather)
   grid_dependency_wait();
   grid_dependency_trigger();
   const int tid = threadIdx.x;
-  if (a.reset_err) {   // the call's first kernel clears the error word itself
+  // CTA 0 writes the tables and flags bad ids; with the fused row gather the
+  // other CTAs recompute the same order and copy rows
+  const bool tables = blockIdx.x == 0;
+  const bool gather = a.x != nullptr;
+  if (a.reset_err && tables) {   // the call's first kernel clears the error word itself
     if (tid == 0) a.hdr->err = 0;
     __syncthreads();
   }
@@ -335,10 +346,11 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
   if (f < a.n) {
     const int e = a.topk_ids ? a.topk_ids[f] : 0;
     const int l = a.lora_ignore ? -1 : a.lora_ids[f / a.k];
-    if (e < 0 || e >= a.E || l < -1 || l >= a.L)
-      flag_error(&a.hdr->err, kStatusBadIndex);
-    else
+    if (e < 0 || e >= a.E || l < -1 || l >= a.L) {
+      if (tables) flag_error(&a.hdr->err, kStatusBadIndex);
+    } else {
       bin = e * (a.L + 1) + l + 1;
+    }
   }
   for (int b = tid; b < a.nbins; b += blockDim.x) sm_bins[b] = 0;
   __syncthreads();
@@ -354,20 +366,40 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
     }
     __syncthreads();
   }
-  align_tables(a, warp_sums, sm_bins);
+  align_tables(a, warp_sums, sm_bins, tables);
   __syncthreads();
+  int* sm_pos = sm_bins + a.nbins;
   if (f < a.n) {
-    if (bin < 0) {
-      if (a.pos_of) a.pos_of[f] = -1;
-    } else {
-      const int pos = sm_bins[bin] + rank;
-      a.sorted_ids[pos] = f;
-      if (a.row_tok) {
-        a.row_tok[pos] = f / a.k;
-        a.row_lora[pos] = bin % (a.L + 1) - 1;
-        a.row_w[pos] = a.topk_weights ? a.topk_weights[f] : 1.0f;
-        a.pos_of[f] = pos;
+    const int pos = bin < 0 ? -1 : sm_bins[bin] + rank;
+    if (gather) sm_pos[f] = pos;
+    if (tables) {
+      if (bin < 0) {
+        if (a.pos_of) a.pos_of[f] = -1;
+      } else {
+        a.sorted_ids[pos] = f;
+        if (a.row_tok) {
+          a.row_tok[pos] = f / a.k;
+          a.row_lora[pos] = bin % (a.L + 1) - 1;
+          a.row_w[pos] = a.topk_weights ? a.topk_weights[f] : 1.0f;
+          a.pos_of[f] = pos;
+        }
       }
+    }
+  }
+  if (gather && (gridDim.x == 1 || !tables)) {
+    // rows of the entries, 16-byte pieces spread over the copying CTAs
+    // (CTAs 1.. when there are several); padding rows are not written
+    __syncthreads();
+    const int copiers = gridDim.x > 1 ? static_cast<int>(gridDim.x) - 1 : 1;
+    const int ci = gridDim.x > 1 ? static_cast<int>(blockIdx.x) - 1 : 0;
+    const long long total = static_cast<long long>(a.n) * a.hv;
+    for (long long i = static_cast<long long>(ci) * blockDim.x + tid; i < total;
+         i += static_cast<long long>(copiers) * blockDim.x) {
+      const int fe = static_cast<int>(i / a.hv);
+      const int u = static_cast<int>(i - static_cast<long long>(fe) * a.hv);
+      const int pos = sm_pos[fe];
+      if (pos >= 0)
+        a.x_perm[static_cast<size_t>(pos) * a.hv + u] = a.x[static_cast<size_t>(fe / a.k) * a.hv + u];
     }
   }
 }
@@ -544,10 +576,22 @@ bool align_small_fits(const AlignArgs& a) {
   return a.n <= kScanThreads && a.nbins <= kSmallMaxBins && a.E <= kScanThreads;
 }
 
-cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained) {
+cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained, int num_sms) {
   const int threads = (std::max(std::max(a.n, a.E), 32) + 31) / 32 * 32;
-  return launch_chained(align_small_kernel, dim3(1), dim3(threads), a.nbins * sizeof(int), stream,
-                        chained, a);
+  const bool gather = a.x != nullptr && a.logits == nullptr;
+  AlignArgs b = a;
+  if (!gather) {
+    b.x = nullptr;
+    b.x_perm = nullptr;
+  }
+  int grid = 1;
+  if (gather) {   // one table CTA plus copiers of about four pieces per thread
+    const long long pieces = static_cast<long long>(a.n) * a.hv;
+    grid = 1 + static_cast<int>(std::min<long long>((pieces + 4LL * threads - 1) / (4LL * threads),
+                                                    std::max(1, num_sms - 1)));
+  }
+  const size_t smem = (static_cast<size_t>(a.nbins) + (gather ? a.n : 0)) * sizeof(int);
+  return launch_chained(align_small_kernel, dim3(grid), dim3(threads), smem, stream, chained, b);
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
