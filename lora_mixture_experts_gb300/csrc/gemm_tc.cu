@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.r > 0) {
       tma_prefetch_desc(&maps.lb);
       tma_prefetch_desc(&maps.la);
+      tma_prefetch_desc(&maps.la_run);
     }
   }
   if (warp == 1) {
@@ -337,6 +338,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ns1 = PAIR ? max(0, si.nslot - spc) : 0;
           const int ns_me = rank == 0 ? ns0 : ns1;
           const uint32_t per_kb = (ns0 + ns1) * p.r * 128 + (PAIR ? 2 : 1) * brows * 128;
+          // a full set of slots on consecutive adapters comes in one box of
+          // 128 rows (small per-adapter boxes had made shrink items slow)
+          int a_run = -1;
+          if (ns_me == spc) {
+            const int* sa = p.slot_adapter + si.slot0 + static_cast<int>(rank) * spc;
+            a_run = sa[0];
+            for (int q = 1; q < ns_me; ++q)
+              if (sa[q] != a_run + q) a_run = -1;
+          }
           for (int kb0 = 0; kb0 < nk && ok; kb0 += C::kKB, advance()) {
             const int nkb = min(C::kKB, nk - kb0);
             const int s = sidx;
@@ -346,9 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
               const int kc = kb0 + j;
-              for (int q = 0; q < ns_me; ++q)
-                load4(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
-                      p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
+              if (a_run >= 0) {
+                load4(st + C::a_off(j), &maps.la_run, fb, kc * 64, 0, ti.expert, a_run);
+              } else {
+                for (int q = 0; q < ns_me; ++q)
+                  load4(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
+                        p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
+              }
               if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
             if (!waited && ++n_def == C::kStages) load_deferred_rows(nk, 0, 0, tb, brow0);

@@ -13,6 +13,7 @@ struct alignas(64) GemmMaps {
   CUtensorMap w;      // base weights, 3D (K, rows, E); gate_up: 4D (K, I, 2, E)
   CUtensorMap lb;     // LoRA expand weights B, 4D (r, rows, E, L); gate_up: 5D (r, I, 2, E, L)
   CUtensorMap la;     // LoRA shrink weights A, 4D (K, r, E, L)
+  CUtensorMap la_run; // the same with a box of 128 / r consecutive adapters
   CUtensorMap b[5];   // token operand (x_perm or act), 2D (K, rows)
   CUtensorMap z[5];   // shrink results, 2D (r, slots * tn)
 };

@@ -458,10 +458,10 @@ bool enc_gate_up_lora(CUtensorMap* m, const void* base, uint64_t r, uint64_t I, 
 }
 
 bool enc4(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
-          uint32_t b0, uint32_t b1) {
+          uint32_t b0, uint32_t b1, uint32_t b3 = 1) {
   const uint64_t dims[4] = {d0, d1, d2, d3};
   const uint64_t str[3] = {d0, d0 * d1, d0 * d1 * d2};
-  const uint32_t box[4] = {b0, b1, 1, 1};
+  const uint32_t box[4] = {b0, b1, 1, b3};
   return encode_map(m, base, 4, dims, str, box);
 }
 
@@ -774,6 +774,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   if (p.lora) {
     ok = ok && enc_gate_up_lora(&mg.lb, B_gu, p.r, p.I, p.E, p.L, lw);
     ok = ok && enc4(&mg.la, A_gu, p.H, p.r, p.E, p.L, 64, p.r);
+    ok = ok && enc4(&mg.la_run, A_gu, p.H, p.r, p.E, p.L, 64, p.r, 128 / p.r);
     ok = ok && enc_row_maps(mg.z, zgu, 2 * p.r, zrows, lw, p.tn);
   }
   // down phase maps
@@ -784,6 +785,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   if (p.lora) {
     ok = ok && enc4(&md.lb, B_d, p.r, p.H, p.E, p.L, lw, 128);
     ok = ok && enc4(&md.la, A_d, p.I, p.r, p.E, p.L, 64, p.r);
+    ok = ok && enc4(&md.la_run, A_d, p.I, p.r, p.E, p.L, 64, p.r, 128 / p.r);
     ok = ok && enc_row_maps(md.z, zd, p.r, zrows, lw, p.tn);
   }
   if (!ok) return MOELORA_ERR_CUDA;
@@ -925,6 +927,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   if (p.lora) {
     ok = ok && enc4(&m.lb, B, p.r, p.N, 1, p.L, lw, 128);
     ok = ok && enc4(&m.la, A, p.H, p.r, 1, p.L, 64, p.r);
+    ok = ok && enc4(&m.la_run, A, p.H, p.r, 1, p.L, 64, p.r, 128 / p.r);
     ok = ok && enc_row_maps(m.z, z, p.r, zrows, lw, p.tn);
   }
   if (!ok) return MOELORA_ERR_CUDA;
