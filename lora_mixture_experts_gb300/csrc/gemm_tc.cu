@@ -645,6 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_j = valid ? p.slot_adapter[si.slot0 + j] : -3;
         __nv_bfloat16* zrow =
             p.zbuf + (static_cast<size_t>(si.slot0 + (valid ? j : 0)) * TN) * (p.z_parts * p.r) + q;
+        // the slot's tokens: rows of one expert are sorted by adapter, so they
+        // are the tile's columns [c_lo, c_hi) of the (expert, adapter) bin
+        int c_lo = 0, c_hi = 0;
+        if (valid) {
+          const int b = ti.expert * p.lp1 + a_j + 1;
+          c_lo = p.bin_start[b] - ti.row0;
+          c_hi = a_j + 2 < p.lp1 ? p.bin_start[b + 1] - ti.row0 : ti.nrows;
+          c_hi = min(c_hi, ti.nrows);
+        }
         for (int c0 = 0; c0 < nmma; c0 += 16) {
           float v[16];
           tmem_ld16(t_row + c0, v);
@@ -652,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc) {
               const int c = c0 + cc;
-              const bool keep = c < ti.nrows && p.row_lora[ti.row0 + c] == a_j;
+              const bool keep = c >= c_lo && c < c_hi;
               const float z = keep ? v[cc] : 0.0f;
               const __nv_bfloat16 hi = __float2bfloat16_rn(z);
               zrow[static_cast<size_t>(c) * (p.z_parts * p.r)] = hi;

@@ -42,6 +42,8 @@ struct GemmParams {
   const ShrinkItem* shrink;
   const int* slot_adapter;
   const int* row_lora;
+  const int* bin_start;   // first sorted row of each (expert, adapter + 1) bin
+  int lp1;                // adapter bins per expert (L + 1)
   const float* row_w;
   const int* row_tok;
   int* tile_done;

@@ -636,6 +636,8 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   g.shrink = a.shrink;
   g.slot_adapter = a.slot_adapter;
   g.row_lora = a.row_lora;
+  g.bin_start = a.bin_start;
+  g.lp1 = p.L + 1;
   g.row_w = a.row_w;
   g.row_tok = a.row_tok;
   g.tile_done = a.tile_done;
