@@ -251,6 +251,43 @@ def test_forward_deterministic_and_graph_capturable():
     assert torch.equal(out, a)
 
 
+def test_back_to_back_calls_on_one_stream():
+    # Calls of different shapes (small-batch path with the fused row gather,
+    # the multi-kernel align path, the dense linear) queued on one stream
+    # without a synchronisation in between, some sharing a workspace: every
+    # launch may begin before its predecessor ends, so each result must still
+    # equal the same call made alone.
+    small = make_moe_case(CONFIGS["tiny"], seed=3, device=DEV)
+    big_c = small_moe_case(1100, 128, 192, 8, 2, 3, 32)   # > 1024 entries: hist/scan/scatter align
+    big = make_moe_case(big_c, seed=4, device=DEV)
+    lin_c = CONFIGS["dense_t8"]
+    lin = make_linear_case(lin_c, seed=5, device=DEV)
+
+    def ws_for(d):
+        dims = binding.dims_of(d["x"], d["topk_ids"], d["W_gate_up"], d["W_down"], d["A_gu"])
+        return binding.alloc_workspace(binding.moelora_workspace_bytes(dims))
+
+    ws_small, ws_big = ws_for(small), ws_for(big)
+    alone = {}
+    alone["small"] = _gpu_forward(small, ws=ws_small).clone()
+    alone["big"] = _gpu_forward(big, ws=ws_big).clone()
+    alone["lin"] = binding.moe_lora_linear(lin["x"], lin["lora_ids"], lin["W"], lin["A"], lin["B"]).clone()
+    torch.cuda.synchronize()
+
+    small2 = dict(small, lora_ids=torch.roll(small["lora_ids"], 1))   # other routing, same workspace
+    outs = []
+    for _ in range(3):
+        outs.append(("small", _gpu_forward(small, ws=ws_small)))
+        outs.append(("big", _gpu_forward(big, ws=ws_big)))
+        outs.append(("small2", _gpu_forward(small2, ws=ws_small)))
+        outs.append(("lin", binding.moe_lora_linear(lin["x"], lin["lora_ids"], lin["W"], lin["A"], lin["B"])))
+    torch.cuda.synchronize()
+    alone["small2"] = _gpu_forward(small2, ws=ws_small).clone()
+    torch.cuda.synchronize()
+    for name, out in outs:
+        assert torch.equal(out, alone[name]), name
+
+
 def test_forward_bad_index_flag():
     d = make_moe_case(CONFIGS["tiny"], seed=0, device=DEV)
     dims = binding.dims_of(d["x"], d["topk_ids"], d["W_gate_up"], d["W_down"], d["A_gu"])
