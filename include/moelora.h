@@ -113,7 +113,7 @@ int moe_lora_align(const moelora_dims* d, const int32_t* topk_ids_dev,
 /*
  * moe_lora_align_noalloc -- moe_lora_align without a workspace argument.
  *
- * The paper has no counterpart: this exists for callers that cannot
+ * The multi-LoRA MoE blog describes no such call: it exists for callers that cannot
  * allocate device memory -- code running while a stream is captured into a
  * CUDA graph (a cudaMalloc there breaks the capture), plug-ins handed
  * tensors but no allocator, and servers that reserved all device memory for

@@ -35,8 +35,11 @@ Pins (tests under ``tests/test_oracle_pins.py``): a hand-derived closed-form
 example, a scalar brute force on tiny shapes, the merged-weight identity
 x(W + AB) = xW + xAB, adapter -1 / B = 0 reducing to the plain MoE, E = 1
 top-1 reducing to a dense two-projection MLP, linearity in the gate weights,
-the align definition checked by a counting sort and its invariants, and the
-router against a two-expert closed form and a library top-k.
+the align definition checked by a counting sort and its invariants, the
+router against a two-expert closed form and a library top-k, per-token
+independence, and the bf16 widening against the format's definition.  The
+same tests rewrite single expressions of this file (swapped operands, dropped
+terms, wrong indices) and check that some pin fails for each rewrite.
 """
 from __future__ import annotations
 

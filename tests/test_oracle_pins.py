@@ -11,10 +11,15 @@ fix, independent of the oracle's own code path.
   and the dense linear to x W^T + per-adapter LoRA;
 * linearity of the combine in the gate weights (one-hot weights isolate one
   expert);
-* the align step against a counting sort and its invariants.
+* the align step against a counting sort and its invariants;
+* the router against a two-expert closed form and a library top-k;
+* per-token independence (any subset of tokens gives the matching rows);
+* the bf16 -> float64 widening against the format's definition.
 
-The last test plants mistakes in the oracle (on the CPU) and checks that at
-least one pin catches each one.
+The last tests plant mistakes in the oracle (on the CPU): monkeypatched
+helpers, and 21 source-level rewrites of single expressions (swapped gate/up
+halves, LoRA shared across experts, a dropped gate weight, a wrong index or
+comparison in the align, ...).  Each must make at least one pin fail.
 """
 import json
 import math
@@ -261,27 +266,36 @@ def pin_router(seed=6):
     return bool(ok)
 
 
+def pin_token_subset(seed=7):
+    """Each token's output depends only on its own routing and adapter: any
+    subset of tokens, in any order, gives the matching rows of the full
+    evaluation (with adapters, so a per-token index slip shows)."""
+    rng = np.random.default_rng(seed)
+    d = _rand_layer(rng, T=12, H=8, I=6, E=4, k=2, L=2, r=2)
+    full = _fwd(d)
+    ok = True
+    for sub in ([7, 2, 11], [11, 10, 9, 8], [0]):
+        ok &= _rel(_fwd(d, tokens=sub), full[sub]) < 1e-13
+    return bool(ok)
+
+
+def pin_bf16_conversion():
+    """bf16 bit patterns widen exactly: the value is the float32 whose upper
+    16 bits are the pattern (sign, 8-bit exponent, 7-bit mantissa)."""
+    bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x8000, 0x7F7F, 0x0001], dtype=np.uint16)
+    exp = [1.0, -1.0, 3.140625, 0.0, -0.0, (2 - 2 ** -7) * 2.0 ** 127, 2.0 ** -133]
+    got = ref.as_f64(bits).tolist()
+    return got == exp and math.copysign(1.0, got[4]) == -1.0
+
+
 PINS = [pin_closed_form, pin_brute_force, pin_merged_identity, pin_base_moe,
-        pin_dense_reduction, pin_linearity, pin_align, pin_router]
+        pin_dense_reduction, pin_linearity, pin_align, pin_router, pin_token_subset,
+        pin_bf16_conversion]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
 def test_oracle_pin(pin):
     assert pin()
-
-
-def test_oracle_token_subset():
-    rng = np.random.default_rng(7)
-    d = _rand_layer(rng, T=12, H=8, I=6, E=4, k=2, L=2, r=2)
-    full = _fwd(d)
-    sub = [7, 2, 11]
-    assert _rel(_fwd(d, tokens=sub), full[sub]) < 1e-13
-
-
-def test_oracle_bf16_conversion_exact():
-    bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x8000, 0x7F7F], dtype=np.uint16)
-    exp = [1.0, -1.0, 3.140625, 0.0, -0.0, 3.3895313892515355e38]
-    assert ref.as_f64(bits).tolist() == exp
 
 
 def test_oracle_rejects_bad_ids():
@@ -325,3 +339,72 @@ def test_pins_catch_align_mistake(monkeypatch):
     # drop the flat-index tie break (unstable order within a segment)
     monkeypatch.setattr(np, "lexsort", lambda keys: orig((-keys[0],) + tuple(keys[1:])))
     assert not pin_align()
+
+
+# ------------------------------------------------ source-level mutations
+# Each mutation rewrites one expression of the oracle's source (a swapped
+# operand, a dropped term, a wrong index or comparison) and runs every pin on
+# the rewritten module: at least one pin must fail or raise.
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "oracle", "moe_lora_ref.py")
+
+SOURCE_MUTATIONS = {
+    "gate_up_halves_swapped": ("act = silu(g[:, :I]) * g[:, I:]", "act = silu(g[:, I:]) * g[:, :I]"),
+    "silu_on_both_halves": ("act = silu(g[:, :I]) * g[:, I:]", "act = silu(g[:, :I]) * silu(g[:, I:])"),
+    "gu_lora_shared_across_experts": ("as_f64(A_gu[a, e]), as_f64(B_gu[a, e])",
+                                      "as_f64(A_gu[a, 0]), as_f64(B_gu[a, 0])"),
+    "d_lora_shared_across_experts": ("as_f64(A_d[a, e]), as_f64(B_d[a, e])",
+                                     "as_f64(A_d[a, 0]), as_f64(B_d[a, 0])"),
+    "down_lora_reads_gate": ("_lora_delta(act[m],", "_lora_delta(g[m][:, :I],"),
+    "down_lora_dropped": ("d[m] += _lora_delta(act[m]", "d[m] += 0 * _lora_delta(act[m]"),
+    "gate_up_lora_after_activation": ("g[m] += _lora_delta(Xe[m]", "g[m] += 0 * _lora_delta(Xe[m]"),
+    "gate_weight_dropped": ("out[i] += topk_weights[t, j] * pair_d[(i, j)]", "out[i] += pair_d[(i, j)]"),
+    "gate_weight_of_first_expert": ("out[i] += topk_weights[t, j] *", "out[i] += topk_weights[t, 0] *"),
+    "adapter_indexed_by_subset_row": ("ae = lora_ids[tokens[rows]]", "ae = lora_ids[rows]"),
+    "token_indexed_by_subset_row": ("Xe = x[tokens[rows]]", "Xe = x[rows]"),
+    "expand_uses_shrink_matrix": ("return z @ B.T", "return z @ A[:, :B.shape[0]].T if A.shape[1] >= B.shape[0] else z @ B.T"),
+    "bf16_bits_misplaced": ("<< 16", "<< 15"),
+    "silu_sign": ("v / (1.0 + np.exp(-v))", "v / (1.0 + np.exp(v))"),
+    "align_unstable": ("np.lexsort((f_of, a_of + 1, e_of))", "np.lexsort((-f_of, a_of + 1, e_of))"),
+    "align_adapters_reversed": ("np.lexsort((f_of, a_of + 1, e_of))", "np.lexsort((f_of, -a_of, e_of))"),
+    "align_seg_off_inclusive": ("np.count_nonzero(a_of[mine] < a)", "np.count_nonzero(a_of[mine] <= a)"),
+    "align_exact_multiple_overpadded": ("pad = -(-count // block_m) * block_m",
+                                        "pad = (count // block_m + 1) * block_m"),
+    "router_ties_to_higher_index": ("(-float(logits[t, e]), e)", "(-float(logits[t, e]), -e)"),
+    "router_weights_not_renormalised": ("w[t] = sel / sel.sum()", "w[t] = sel / np.exp(lt - lt.max()).sum()"),
+    "linear_adapter_ignored": ("_lora_delta(x[m], as_f64(A[a]), as_f64(B[a]))",
+                               "_lora_delta(x[m], as_f64(A[0]), as_f64(B[0]))"),
+}
+
+
+def _oracle_from_source(src):
+    import types
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src, ORACLE_SRC, "exec"), mod.__dict__)
+    return mod
+
+
+def _run_pins(monkeypatch, mod):
+    import sys
+    monkeypatch.setattr(sys.modules[__name__], "ref", mod)
+    results = {}
+    for p in PINS:
+        try:
+            results[p.__name__] = bool(p())
+        except Exception as exc:            # a mutant that raises is caught too
+            results[p.__name__] = f"raised {type(exc).__name__}"
+    return results
+
+
+def test_unmutated_source_passes_every_pin(monkeypatch):
+    res = _run_pins(monkeypatch, _oracle_from_source(open(ORACLE_SRC).read()))
+    assert all(v is True for v in res.values()), res
+
+
+@pytest.mark.parametrize("name", sorted(SOURCE_MUTATIONS))
+def test_pins_catch_source_mutation(monkeypatch, name):
+    old, new = SOURCE_MUTATIONS[name]
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation site not unique: {old!r}"
+    res = _run_pins(monkeypatch, _oracle_from_source(src.replace(old, new)))
+    assert not all(v is True for v in res.values()), res
