@@ -51,6 +51,9 @@ def test_workspace_sizes(lib):
     assert binding.moelora_workspace_bytes(_d(k=40)) == 0          # k > E
     assert binding.moelora_workspace_bytes(_d(H=2884)) == 0        # H % 8
     assert binding.moelora_workspace_bytes(_d(r=24)) == 0          # rank not supported
+    assert binding.moelora_workspace_bytes(_d(E=1024, L=10, k=4)) > 0   # 11264 bins: the limit
+    assert binding.moelora_workspace_bytes(_d(E=1024, L=11, k=4)) == 0  # 12288 bins
+    assert binding.moelora_workspace_bytes(_d(E=1025, L=0, r=0, k=4)) == 0
     assert binding.moelora_linear_workspace_bytes(moelora_linear_dims(512, 8192, 28672, 32, 16)) > 0
     assert binding.moelora_align_capacity(_d(), 16) == 16 * 4 + 32 * 15
     assert binding.moelora_align_capacity(_d(), 0) == 0
@@ -72,6 +75,8 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, _d(r=40)) == UNSUP
     assert _fwd(lib, _d(r=144)) == UNSUP
     assert _fwd(lib, _d(E=2048, k=2)) == UNSUP
+    assert _fwd(lib, _d(E=1024, L=11, k=4)) == UNSUP             # E*(L+1) above 11264
+    assert _fwd(lib, _d(T=1 << 28, k=4)) == UNSUP                # T*k reaches 2^30
     p = [ctypes.c_void_p(FAKE)] * 11
     p[0] = None                                              # x
     assert _fwd(lib, _d(), p) == INVALID

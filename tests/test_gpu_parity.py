@@ -86,6 +86,17 @@ def test_align_large_shapes():
     _check_align(ids, lo, 256, 4, 16)
 
 
+def test_align_maximum_bins():
+    """E = 1024 experts and L = 10 adapters: E*(L+1) = 11264 bins, the most the
+    library accepts; a tiny batch (too many bins for the single-CTA path) and
+    a 16384-entry batch."""
+    g = torch.Generator().manual_seed(11)
+    for T, k in ((5, 3), (2048, 8)):
+        ids = torch.stack([torch.randperm(1024, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+        lo = torch.randint(-1, 10, (T,), generator=g, dtype=torch.int32)
+        _check_align(ids, lo, 1024, 10, 16)
+
+
 def test_align_bad_index_flag():
     ids = torch.tensor([[0, 1], [1, 7]], dtype=torch.int32, device=DEV)
     lo = torch.tensor([0, -1], dtype=torch.int32, device=DEV)
@@ -208,6 +219,18 @@ def test_forward_many_experts_top8():
     d = make_moe_case(c, seed=6, device=DEV)
     rng = np.random.default_rng(3)
     _run_parity(d, tokens=np.sort(rng.choice(1024, size=64, replace=False)), what="E64 top-8")
+
+
+def test_forward_maximum_bins_and_top32():
+    """The largest expert x adapter table (E = 1024, L = 10: 11264 bins) and
+    the largest top-k the router kernel takes (k = 32)."""
+    c = small_moe_case(1500, 64, 128, 1024, 4, 10, 16, routing="zipf")
+    d = make_moe_case(c, seed=12, device=DEV)
+    rng = np.random.default_rng(12)
+    _run_parity(d, tokens=np.sort(rng.choice(1500, size=48, replace=False)), what="E1024 L10")
+    c = small_moe_case(96, 128, 64, 64, 32, 3, 32)
+    d = make_moe_case(c, seed=13, device=DEV)
+    _run_parity(d, what="top-32")
 
 
 def test_forward_empty_batch():
