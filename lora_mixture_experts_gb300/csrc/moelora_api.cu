@@ -101,14 +101,17 @@ bool parse_tune_line(const std::string& line, TuneEntry& e, bool& is_entry) {
     const std::string key = tok.substr(0, eq), val = tok.substr(eq + 1);
     char* end = nullptr;
     if (key == "T") {
+      // a value or lo-hi, both plain decimal numbers
       const size_t dash = val.find('-');
-      e.t_lo = static_cast<int>(std::strtol(val.c_str(), &end, 10));
-      if (dash == std::string::npos) {
-        e.t_hi = e.t_lo;
-      } else {
-        e.t_hi = static_cast<int>(std::strtol(val.c_str() + dash + 1, &end, 10));
-      }
-      if (e.t_lo < 0 || e.t_hi < e.t_lo) return false;
+      const std::string lo = val.substr(0, dash);
+      const std::string hi = dash == std::string::npos ? lo : val.substr(dash + 1);
+      if (lo.empty() || hi.empty() || lo.size() > 9 || hi.size() > 9 ||
+          lo.find_first_not_of("0123456789") != std::string::npos ||
+          hi.find_first_not_of("0123456789") != std::string::npos)
+        return false;
+      e.t_lo = std::atoi(lo.c_str());
+      e.t_hi = std::atoi(hi.c_str());
+      if (e.t_hi < e.t_lo) return false;
       continue;
     }
     const long v = std::strtol(val.c_str(), &end, 10);

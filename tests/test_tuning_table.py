@@ -67,7 +67,8 @@ def test_folder_loads_every_cfg_in_name_order(tmp_path):
     assert binding.moelora_workspace_bytes(DEC) == only1         # a.cfg came first
 
 
-@pytest.mark.parametrize("text", ["moe tn=48\n", "moe ksplit=9\n", "attention T=4\n", "moe T=9-3\n", "moe bogus=1\n", "moe T\n"])
+@pytest.mark.parametrize("text", ["moe tn=48\n", "moe ksplit=9\n", "attention T=4\n", "moe T=9-3\n", "moe bogus=1\n",
+                                  "moe T\n", "moe T=x\n", "moe T=5x\n", "moe T=-3\n", "moe T=4-\n", "moe k=4q\n"])
 def test_malformed_tables_are_rejected_and_keep_the_old_one(tmp_path, text):
     binding.moelora_load_tuning(_write(tmp_path, "ok.cfg", "moe ksplit=1\n"))
     with pytest.raises(MoeLoraError):
