@@ -380,17 +380,29 @@ def run_ours(args, rank, world, device):
         achieved, peak, unit = w.flops / dur_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
     traffic = load_traffic(args.config, dom)
 
-    # end to end through the public API: inputs from pinned host memory,
-    # result read back, every step
-    host = {k: d[k].cpu().pin_memory() for k in step_inputs}
-    dev_in = {k: torch.empty_like(d[k]) for k in step_inputs}
+    # end to end through the public API: the step's inputs packed in one
+    # pinned host buffer (each at a 256-byte offset) and copied in one
+    # transfer, the forward on device views of that buffer, the result read
+    # back, every step
+    offs, nbytes = {}, 0
+    for k in step_inputs:
+        offs[k] = nbytes
+        nbytes += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
+    host_buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev_buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def view(buf, k):
+        n = d[k].numel() * d[k].element_size()
+        return buf[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
+    for k in step_inputs:
+        view(host_buf, k).copy_(d[k].cpu())
+    dev_in = {k: view(dev_buf, k) for k in step_inputs}
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d = nbytes
     d2h = out.numel() * out.element_size()
 
     def e2e_step():
-        for k in step_inputs:
-            dev_in[k].copy_(host[k], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         fwd(*[dev_in[k] for k in step_inputs])
         out_h.copy_(out, non_blocking=True)
     for _ in range(min(args.warmup, 5)):
