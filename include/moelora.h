@@ -24,7 +24,14 @@
  *  - Return value: MOELORA_OK (0) or a negative MOELORA_ERR_* code.  Argument
  *    errors are reported before anything is enqueued.  Errors found by the
  *    kernels (bad ids, a bounded wait that ran out) are recorded in the
- *    workspace and read back with moelora_get_error.
+ *    workspace and read back with moelora_get_error.  Every wait in the
+ *    kernels gives up after 2 s; the kernel then winds down and the next
+ *    call runs normally.  Setting the environment variable
+ *    MOELORA_FAULT_INJECT=shrink_wait makes the first GEMM phase of each
+ *    call wait for shrink results that never come, so that a test can see
+ *    MOELORA_ERR_TIMEOUT (the output of such a call is undefined).
+ *  - The workspace needs no initialisation: every byte a call reads was
+ *    written earlier in the same call.
  *  - Not thread-safe per workspace: two calls that share a workspace must be
  *    ordered on one stream.
  */

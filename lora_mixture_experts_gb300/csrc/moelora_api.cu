@@ -69,6 +69,17 @@ int env_override(const char* name, int lo, int hi) {
   return (x >= lo && x <= hi) ? x : 0;
 }
 
+// Failure-detection test hook: with MOELORA_FAULT_INJECT=shrink_wait the
+// first GEMM phase of a call (gate_up, or the dense linear's only phase)
+// waits for twice the shrink completions its tiles will ever see.  Its
+// bounded counter wait then runs out (after the library's 2 s wait limit),
+// the kernel winds down, and moelora_get_error reports MOELORA_ERR_TIMEOUT;
+// nothing faults or hangs, and the next call runs normally.
+int first_phase_done_target() {
+  const char* v = std::getenv("MOELORA_FAULT_INJECT");
+  return v && std::strcmp(v, "shrink_wait") == 0 ? 2 : 1;
+}
+
 // ------------------------------------------------------------ tuning table
 // Lines of `key=value` tokens, '#' starts a comment.  The first token is the
 // entry kind (`moe` or `linear`); shape keys T (a value or a range lo-hi),
@@ -802,7 +813,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   const bool paired = moe_gemm_paired(p.tn);
   gu.n_mtiles = (p.I + (paired ? 127 : 63)) / (paired ? 128 : 64);
   gu.out_feats = p.I;
-  gu.done_target = 1;
+  gu.done_target = first_phase_done_target();
   const int units = paired ? sms / 2 : sms;
   const double rows_per_expert = static_cast<double>(p.n) / p.E;
   gu.group_tiles = group_tiles(p.tn, gu.n_mtiles, rows_per_expert, units);
@@ -942,7 +953,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   const bool paired = moe_gemm_paired(p.tn);
   g.n_mtiles = (p.N + (paired ? 255 : 127)) / (paired ? 256 : 128);
   g.out_feats = p.N;
-  g.done_target = 1;
+  g.done_target = first_phase_done_target();
   g.group_tiles = group_tiles(p.tn, g.n_mtiles, static_cast<double>(p.T), paired ? sms / 2 : sms);
   g.zbuf = z;
   g.out_ld = p.N;
