@@ -47,8 +47,10 @@ struct AlignArgs {
   // token tiles, LoRA slots and shrink items for the GEMM phases
   int tn;                       // token tile width
   int spi;                      // slots per shrink item (128 / r); 0 = no LoRA
+  int sks;                      // K splits of every shrink item (>= 1)
   TileInfo* tiles;
-  ShrinkItem* shrink;
+  ShrinkItem* shrink;           // [shrink items * sks], the splits of an item adjacent
+  int* sh_cnt;                  // [2 * shrink items] split arrivals per item and CTA of a pair
   int* slot_adapter;
   int* tile_done;
   // 1: the single-CTA align zeroes the workspace error word before anything

@@ -246,7 +246,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
       ti.row0 = s0;
       ti.nrows = s1 - s0;
       ti.slot_base = sl;
-      ti.sh_base = sh;
+      ti.sh_base = sh * a.sks;
       ti.pad_ = 0;
       int ns = 0;
       if (a.spi > 0) {
@@ -264,8 +264,12 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
         si.tile = tbase + j;
         si.slot0 = sl + h * a.spi;
         si.nslot = min(a.spi, ns - h * a.spi);
-        si.pad_ = 0;
-        a.shrink[sh + h] = si;
+        for (int s = 0; s < a.sks; ++s) {
+          si.ks = s;
+          a.shrink[(sh + h) * a.sks + s] = si;
+        }
+        a.sh_cnt[2 * (sh + h)] = 0;
+        a.sh_cnt[2 * (sh + h) + 1] = 0;
       }
       a.tiles[tbase + j] = ti;
       a.tile_done[tbase + j] = 0;
@@ -276,7 +280,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
   if (tid == 0) {
     a.hdr->n_tiles = tot_t;
     a.hdr->n_slots = tot_s;
-    a.hdr->n_shrink = tot_h;
+    a.hdr->n_shrink = tot_h * a.sks;
     a.hdr->work[0] = 0;
     a.hdr->work[1] = 0;
   }

@@ -24,12 +24,14 @@ struct TileInfo {
   int pad_;
 };
 
-// One shrink item: the LoRA shrink of up to 128/r slots of one tile.
+// One shrink item: the LoRA shrink of up to 128/r slots of one tile, over
+// one of the K splits of the shrink (the splits of an item are adjacent in
+// the table; the last one to finish sums their partial results).
 struct ShrinkItem {
   int tile;
   int slot0;      // first global slot
   int nslot;      // slots in this item
-  int pad_;
+  int ks;         // K split, 0 .. shrink splits - 1
 };
 
 // Device-side counters and scalars at the head of the workspace.

@@ -89,6 +89,11 @@ struct Cfg {
   }
 };
 
+// First K block of split s when nk blocks are cut into n splits.
+__device__ __forceinline__ int split_begin(int nk, int s, int n) {
+  return static_cast<int>(static_cast<long long>(nk) * s / n);
+}
+
 struct Item {
   int shrink;   // 1 = shrink item
   int tile;
@@ -347,8 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 1; q < ns_me; ++q)
               if (sa[q] != a_run + q) a_run = -1;
           }
-          for (int kb0 = 0; kb0 < nk && ok; kb0 += C::kKB, advance()) {
-            const int nkb = min(C::kKB, nk - kb0);
+          // this item's K split of the shrink
+          const int kb_lo = split_begin(nk, si.ks, p.sh_splits);
+          const int kb_hi = split_begin(nk, si.ks + 1, p.sh_splits);
+          for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += C::kKB, advance()) {
+            const int nkb = min(C::kKB, kb_hi - kb0);
             const int s = sidx;
             uint32_t fb;
             if (!(ok = acquire(s, sph, fb))) break;
@@ -365,9 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
-            if (!waited && ++n_def == C::kStages) load_deferred_rows(nk, 0, 0, tb, brow0);
+            if (!waited && ++n_def == C::kStages)
+              load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0);
           }
-          if (!waited) load_deferred_rows(nk, 0, 0, tb, brow0);
+          if (!waited) load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0);
         } else {
           const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
           const int kc0 = p.split_k0[it.ks];
@@ -483,7 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + buf * TN;
         const int nl =
             (!it.shrink && p.r > 0 && it.ks == p.ksplit - 1) ? ti.nslots * p.lora_chunks * p.z_parts : 0;
-        const int nb = it.shrink ? nk : p.split_k0[it.ks + 1] - p.split_k0[it.ks];
+        int nb;
+        if (it.shrink) {
+          const int sks = p.shrink[it.sh].ks;
+          nb = split_begin(nk, sks + 1, p.sh_splits) - split_begin(nk, sks, p.sh_splits);
+        } else {
+          nb = p.split_k0[it.ks + 1] - p.split_k0[it.ks];
+        }
         const int st_base = (nb + C::kKB - 1) / C::kKB;
         const int cps = p.r > 0 ? C::kKB * 64 / p.lora_w : 1;   // expand chunks per stage
         const int st_all = st_base + (nl + cps - 1) / cps;
@@ -654,28 +669,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           c_hi = a_j + 2 < p.lp1 ? p.bin_start[b + 1] - ti.row0 : ti.nrows;
           c_hi = min(c_hi, ti.nrows);
         }
-        for (int c0 = 0; c0 < nmma; c0 += 16) {
-          float v[16];
-          tmem_ld16(t_row + c0, v);
-          if (valid) {
+        // z of columns c0 .. c0+15 (the slot's tokens kept, zeros elsewhere)
+        auto store_z = [&](const float* v, int c0) {
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) {
-              const int c = c0 + cc;
-              const bool keep = c >= c_lo && c < c_hi;
-              const float z = keep ? v[cc] : 0.0f;
-              const __nv_bfloat16 hi = __float2bfloat16_rn(z);
-              zrow[static_cast<size_t>(c) * (p.z_parts * p.r)] = hi;
-              if (p.z_parts == 2)
-                zrow[static_cast<size_t>(c) * (2 * p.r) + p.r] = __float2bfloat16_rn(z - __bfloat162float(hi));
+          for (int cc = 0; cc < 16; ++cc) {
+            const int c = c0 + cc;
+            const bool keep = c >= c_lo && c < c_hi;
+            const float z = keep ? v[cc] : 0.0f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(z);
+            zrow[static_cast<size_t>(c) * (p.z_parts * p.r)] = hi;
+            if (p.z_parts == 2)
+              zrow[static_cast<size_t>(c) * (2 * p.r) + p.r] = __float2bfloat16_rn(z - __bfloat162float(hi));
+          }
+        };
+        bool last = true;
+        if (p.sh_splits == 1) {
+          for (int c0 = 0; c0 < nmma; c0 += 16) {
+            float v[16];
+            tmem_ld16(t_row + c0, v);
+            if (valid) store_z(v, c0);
+          }
+        } else {
+          // K split: this split's fp32 part of every column, then its
+          // arrival; the split that arrives last (whichever it is) sums the
+          // parts in split order, so the result does not depend on timing
+          const size_t slot = static_cast<size_t>(si.slot0 + (valid ? j : 0));
+          float* part = p.zpart + ((static_cast<size_t>(si.ks) * p.zpart_slots + slot) * TN) * p.r + q;
+          for (int c0 = 0; c0 < nmma; c0 += 16) {
+            float v[16];
+            tmem_ld16(t_row + c0, v);
+            if (valid) {
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) part[static_cast<size_t>(c0 + cc) * p.r] = v[cc];
+            }
+          }
+          named_bar_sync(1, 128);
+          bool mine = false;
+          if (row == 0) {
+            __threadfence();
+            const int before =
+                atomicAdd(&p.sh_cnt[2 * (it.sh / p.sh_splits) + static_cast<int>(rank)], 1);
+            mine = before + 1 == p.done_target * p.sh_splits;
+            __threadfence();
+          }
+          last = bar_red_or(1, 128, mine);
+          if (last && valid) {
+            for (int c0 = 0; c0 < nmma; c0 += 16) {
+              float v[16];
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) v[cc] = 0.0f;
+              for (int s = 0; s < p.sh_splits; ++s) {
+                const float* ps = p.zpart + ((static_cast<size_t>(s) * p.zpart_slots + slot) * TN) * p.r + q;
+#pragma unroll
+                for (int cc = 0; cc < 16; ++cc) v[cc] += __ldcg(ps + static_cast<size_t>(c0 + cc) * p.r);
+              }
+              store_z(v, c0);
             }
           }
         }
-        // publish: every epilogue thread's stores, then one release
-        named_bar_sync(1, 128);
-        if (row == 0) {
-          __threadfence();
-          fence_proxy_async_global();
-          atomicAdd(&p.tile_done[it.tile], 1);
+        if (last) {
+          // publish: every epilogue thread's stores, then one release
+          named_bar_sync(1, 128);
+          if (row == 0) {
+            __threadfence();
+            fence_proxy_async_global();
+            atomicAdd(&p.tile_done[it.tile], 1);
+          }
         }
       } else if (gate_up) {
         // TMEM lane 2i holds gate row i and lane 2i+1 the up row of the same
@@ -834,6 +893,13 @@ size_t moe_gemm_smem_bytes(int tn) {
 }
 
 bool moe_gemm_paired(int tn) { return tn >= 256; }
+
+int moe_gemm_stage_kblocks(int tn) {
+  return tn >= 256 ? Cfg<256, true>::kKB
+                   : (tn >= 128 ? Cfg<128, false>::kKB
+                                : (tn >= 64 ? Cfg<64, false>::kKB
+                                            : (tn >= 32 ? Cfg<32, false>::kKB : Cfg<16, false>::kKB)));
+}
 
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream) {

@@ -47,6 +47,14 @@ struct GemmParams {
   const float* row_w;
   const int* row_tok;
   int* tile_done;
+  // Shrink items split K in sh_splits parts (1 = not split).  Each split
+  // writes its fp32 result to zpart [sh_splits][zpart_slots * tn][r]; the
+  // split whose arrival on sh_cnt (per item and CTA of a pair) comes last
+  // sums the parts in split order and writes zbuf.
+  int sh_splits;
+  float* zpart;
+  int zpart_slots;
+  int* sh_cnt;
   // Shrink results [slots * tn][z_parts * r].  z_parts = 2 keeps each as two
   // bf16 rows, hi = bf16(z) and lo = bf16(z - hi) ([hi r | lo r]), and the
   // expand multiplies both, seeing z to about 16 significant bits: used for
@@ -76,5 +84,8 @@ size_t moe_gemm_smem_bytes(int tn);
 // Whether tiles of this width run on CTA pairs (2-SM MMA): then an item
 // covers 256 weight rows (gate_up: 128 features) instead of 128 (64).
 bool moe_gemm_paired(int tn);
+
+// 64-wide K blocks per pipeline stage for a token-tile width.
+int moe_gemm_stage_kblocks(int tn);
 
 }  // namespace moelora

@@ -39,11 +39,13 @@ struct Plan {
   bool lora = false;
   int n = 0, nbins = 0, nchunks = 0, block_m = kBlockM, Pmax = 0, tn = 32;
   int n_tiles_max = 0, n_slots_max = 0, n_sh_max = 0;
+  int sks = 1;                        // K splits of every shrink item
   int ksplit = 1;                     // K splits of the down / linear phase
   size_t off_hdr = 0, off_chunk_hist = 0, off_bin_of = 0, off_rank_of = 0, off_bin_start = 0;
   size_t off_sorted = 0, off_blk = 0, off_seg = 0;
   size_t off_row_tok = 0, off_row_lora = 0, off_row_w = 0, off_pos_of = 0;
   size_t off_tiles = 0, off_shrink = 0, off_slot_ad = 0, off_tile_done = 0;
+  size_t off_sh_cnt = 0, off_zpart = 0;
   size_t off_xperm = 0, off_zgu = 0, off_zd = 0, off_act = 0, off_ypair = 0;
   size_t off_topk_ids = 0, off_topk_w = 0;   // router results (routed forward)
   size_t total = 0;
@@ -220,6 +222,35 @@ void plan_align_scratch(Plan& p, Bump& b) {
   p.off_bin_start = b.take(static_cast<size_t>(p.nbins) * 4);
 }
 
+// K splits of the shrink items.  A shrink item carries its slots' whole
+// reduction (K = H or I) through the pipeline of one SM while the expand of
+// every main item of its tile waits for it; on weight-streaming (unpaired)
+// tiles that chain is latency-bound, and with a long K it outlasted the main
+// items (E = 1, H = 8192, I = 14336, T = 8: the down phase took 105 us with
+// whole-K shrink items, 53 us with 8 parts).  Split so that a part runs at
+// most kShrinkStages pipeline stages; its fp32 part is summed in split order
+// by the last part to finish.  CTA-pair (tensor-bound) tiles keep one part.
+// MOELORA_SHRINK_SPLITS (1..8) overrides the choice.
+constexpr int kShrinkStages = 8;
+
+int choose_shrink_splits(const Plan& p) {
+  if (!p.lora) return 1;
+  const int kmin = p.linear ? p.H : std::min(p.H, p.I);
+  const int kmax = p.linear ? p.H : std::max(p.H, p.I);
+  int s;
+  if (const int f = env_override("MOELORA_SHRINK_SPLITS", 1, 8)) {
+    s = f;
+  } else if (moe_gemm_paired(p.tn)) {
+    s = 1;
+  } else {
+    const int kkb = moe_gemm_stage_kblocks(p.tn);
+    const int stages = ((kmax + 63) / 64 + kkb - 1) / kkb;
+    s = std::min(8, (stages + kShrinkStages - 1) / kShrinkStages);
+  }
+  // every part gets at least one K block of the shorter phase
+  return std::max(1, std::min(s, (kmin + 63) / 64));
+}
+
 void plan_gemm_tables(Plan& p, Bump& b) {
   p.Pmax = p.n + p.E * (p.block_m - 1);
   // token tile: the smallest of 16/32/64/128/256 rows that holds an average
@@ -234,6 +265,7 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   p.n_tiles_max = p.n / p.tn + std::min(p.E, std::max(p.n, 1)) + 1;
   p.n_slots_max = p.lora ? std::min(p.n, p.E * p.L + p.n_tiles_max) : 0;
   p.n_sh_max = p.n_slots_max;
+  p.sks = choose_shrink_splits(p);
   p.off_sorted = b.take(static_cast<size_t>(p.Pmax) * 4);
   p.off_blk = b.take(static_cast<size_t>(p.Pmax / p.block_m + 1) * 4);
   p.off_seg = b.take(static_cast<size_t>(p.nbins + 1) * 4);
@@ -242,7 +274,8 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   p.off_row_w = b.take(static_cast<size_t>(p.Pmax) * 4);
   p.off_pos_of = b.take(static_cast<size_t>(p.n) * 4);
   p.off_tiles = b.take(static_cast<size_t>(p.n_tiles_max) * sizeof(TileInfo));
-  p.off_shrink = b.take(static_cast<size_t>(std::max(p.n_sh_max, 1)) * sizeof(ShrinkItem));
+  p.off_shrink = b.take(static_cast<size_t>(std::max(p.n_sh_max, 1)) * p.sks * sizeof(ShrinkItem));
+  p.off_sh_cnt = b.take(static_cast<size_t>(std::max(p.n_sh_max, 1)) * 2 * 4);
   p.off_slot_ad = b.take(static_cast<size_t>(std::max(p.n_slots_max, 1)) * 4);
   p.off_tile_done = b.take(static_cast<size_t>(p.n_tiles_max) * 4);
   p.off_xperm = b.take(static_cast<size_t>(p.Pmax) * p.H * 2);
@@ -250,6 +283,9 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   // (the dense linear uses the first half only)
   const size_t zbytes = static_cast<size_t>(p.n_slots_max) * p.tn * p.r * 2 * 2;
   p.off_zgu = b.take(std::max<size_t>(zbytes, 16));
+  // fp32 parts of split shrink results [sks][slots * tn][r]
+  if (p.sks > 1)
+    p.off_zpart = b.take(static_cast<size_t>(p.sks) * p.n_slots_max * p.tn * p.r * 4);
 }
 
 // K splits for the last GEMM phase.  Decode-sized batches have few token
@@ -627,9 +663,16 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
   // item streamed 2 MB while every main item streamed 1 MB.
   const bool paired = moe_gemm_paired(p.tn);
   // slots per shrink item: whole adapters per 128-row tile, on each CTA of a pair
-  a.spi = p.lora ? (paired ? 2 * (128 / p.r) : std::max(1, 128 / (p.r * p.ksplit))) : 0;
+  // (with split shrink items the parts are short anyway: full 128-row stacks,
+  // which keep the number of items down -- the dense T = 64 linear with 8
+  // parts of 2-slot items ran 122 us, with 8 parts of full stacks 116 us)
+  a.spi = p.lora ? (paired ? 2 * (128 / p.r)
+                           : (p.sks > 1 ? 128 / p.r : std::max(1, 128 / (p.r * p.ksplit))))
+                 : 0;
+  a.sks = p.sks;
   a.tiles = ws_ptr<TileInfo>(ws, p.off_tiles);
   a.shrink = ws_ptr<ShrinkItem>(ws, p.off_shrink);
+  a.sh_cnt = ws_ptr<int>(ws, p.off_sh_cnt);
   a.slot_adapter = ws_ptr<int>(ws, p.off_slot_ad);
   a.tile_done = ws_ptr<int>(ws, p.off_tile_done);
 }
@@ -655,6 +698,10 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   g.row_w = a.row_w;
   g.row_tok = a.row_tok;
   g.tile_done = a.tile_done;
+  g.sh_splits = p.sks;
+  g.zpart = p.sks > 1 ? ws_ptr<float>(ws, p.off_zpart) : nullptr;
+  g.zpart_slots = p.n_slots_max;
+  g.sh_cnt = a.sh_cnt;
   return g;
 }
 
@@ -662,7 +709,8 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
 // can be resident at once).
 int gemm_grid(const Plan& p, int n_mtiles, int sms) {
   (void)sms;
-  const long long items = static_cast<long long>(p.n_sh_max) + static_cast<long long>(p.n_tiles_max) * n_mtiles;
+  const long long items = static_cast<long long>(p.n_sh_max) * p.sks +
+                          static_cast<long long>(p.n_tiles_max) * n_mtiles;
   return static_cast<int>(std::max<long long>(1, std::min<long long>(items, 1 << 20)));
 }
 

@@ -18,6 +18,9 @@ with rank 32 and 8 adapters):
                Zipf(1.1) expert load, Zipf adapters with 10% of tokens at -1
 * ``dense``    E=1, top-1, weight 1: x[T,8192] @ W + LoRA r=16 over 32
                adapters, N=28672, T in {1, 8, 64, 512}
+* ``dense_mlp`` the whole layer at E=1, top-1, weight 1 with the dense
+               shapes: H=8192, I=14336 (gate_up 8192 -> 28672, down
+               14336 -> 8192), LoRA r=16 over 32 adapters, T in {1, 8, 64, 512}
 
 Distributions: x ~ N(0,1); a weight with fan-in f ~ N(0, 1/f) (variance
 1/f); A ~ N(0, 1/h_in); B ~ N(0, 1/r), nonzero.  Router logits ~ N(0,1),
@@ -83,6 +86,9 @@ CONFIGS: Dict[str, object] = {
 DENSE_T_SWEEP = (1, 8, 64, 512)
 for _t in DENSE_T_SWEEP:
     CONFIGS[f"dense_t{_t}"] = LinearCase(f"dense_t{_t}", T=_t, K=8192, N=28672, L=32, r=16)
+for _t in DENSE_T_SWEEP:
+    CONFIGS[f"dense_mlp_t{_t}"] = MoECase(f"dense_mlp_t{_t}", T=_t, H=8192, I=14336, E=1, k=1,
+                                          L=32, r=16, adapters="uniform")
 
 
 def bf16_bits(t: torch.Tensor):

@@ -76,13 +76,12 @@ def sweep(names, out_path, device="cuda", log=print):
             case = CONFIGS[name]
             d = (make_linear_case(case, 0, device) if isinstance(case, LinearCase)
                  else make_moe_case(case, 0, device))
-            rows = case.T if isinstance(case, LinearCase) else case.T * case.k / case.E
             make = _runner(case, d, device)
             binding.moelora_load_tuning(None)
             default_ms = _time(make())
             best = None
             for tn in TILES:
-                for ks in ((1, 2, 3, 4) if rows <= 64 else (1,)):
+                for ks in (1, 2, 3, 4):
                     with open(cand_file, "w") as f:
                         f.write(f"{_shape_line(case)} tn={tn} ksplit={ks}\n")
                     binding.moelora_load_tuning(cand_file)

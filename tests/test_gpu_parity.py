@@ -202,6 +202,25 @@ def _random_shapes(n, seed):
     return out
 
 
+SPLIT_SHAPES = [SMALL[4], SMALL[6], SMALL[8], SMALL[9], SMALL[11], SMALL[13]]
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5])
+@pytest.mark.parametrize("shape", SPLIT_SHAPES,
+                         ids=[f"T{s[0]}_H{s[1]}_I{s[2]}_E{s[3]}_k{s[4]}_L{s[5]}_r{s[6]}" for s in SPLIT_SHAPES])
+def test_forward_shrink_split_k(monkeypatch, shape, splits):
+    """Shrink items cut into K splits (forced; the built-in choice splits
+    only long reductions on single-CTA tiles): each split's fp32 part is
+    summed in split order by the last split to finish, on single CTAs and
+    CTA pairs, with the gate_up hi/lo z and every tested rank."""
+    monkeypatch.setenv("MOELORA_SHRINK_SPLITS", str(splits))
+    T, H, I, E, k, L, r = shape
+    d = make_moe_case(small_moe_case(T, H, I, E, k, L, r), seed=21, device=DEV)
+    out = _run_parity(d, what=f"{shape} shrink splits {splits}")
+    again = _gpu_forward(d)
+    assert torch.equal(out, again)          # the order of arrival does not matter
+
+
 @pytest.mark.parametrize("shape", _random_shapes(24, 17), ids=lambda s: "T{T}_H{H}_I{I}_E{E}_k{k}_L{L}_r{r}".format(**s))
 def test_forward_random_shapes(shape):
     s = shape
@@ -231,6 +250,21 @@ def test_forward_maximum_bins_and_top32():
     c = small_moe_case(96, 128, 64, 64, 32, 3, 32)
     d = make_moe_case(c, seed=13, device=DEV)
     _run_parity(d, what="top-32")
+
+
+def test_forward_duplicate_experts_in_topk():
+    """A token may name the same expert more than once in its top-k: each
+    entry is its own routed pair (same expert and adapter, its own gate
+    weight), so the output counts the expert once per entry."""
+    c = small_moe_case(50, 128, 64, 4, 3, 2, 16)
+    d = make_moe_case(c, seed=14, device=DEV)
+    g = torch.Generator().manual_seed(14)
+    ids = torch.randint(0, 4, (50, 3), generator=g, dtype=torch.int32)
+    ids[:10, 1] = ids[:10, 0]              # a pair of equal entries
+    ids[10:15, :] = ids[10:15, :1]         # all three entries equal
+    d["topk_ids"] = ids.to(DEV)
+    _check_align(ids, d["lora_ids"].cpu(), 4, 2, 16)
+    _run_parity(d, what="duplicate experts")
 
 
 def test_forward_empty_batch():
@@ -350,6 +384,22 @@ def test_linear_dense(T, tuned):
     exp = ref.moe_lora_linear_ref(x, lo, W, A, B)
     ok, msg = compare(out[torch.as_tensor(tokens, device=DEV)], exp, f"dense T={T}")
     assert ok, msg
+
+
+@pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
+@pytest.mark.parametrize("T", DENSE_T_SWEEP)
+def test_forward_dense_mlp(T, tuned):
+    """The whole layer at E = 1, top-1 (a dense two-projection MLP with
+    per-token LoRA) with the dense shapes H = 8192, I = 14336."""
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    d = make_moe_case(CONFIGS[f"dense_mlp_t{T}"], seed=0, device=DEV)
+    binding.moelora_load_tuning(table if tuned else None)
+    try:
+        tokens = np.arange(T) if T <= 8 else np.sort(np.random.default_rng(3).choice(T, 8, replace=False))
+        _run_parity(d, tokens=tokens, what=f"dense MLP T={T}")
+    finally:
+        binding.moelora_load_tuning(None)
 
 
 @pytest.mark.parametrize("seed", range(12))
