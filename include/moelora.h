@@ -56,7 +56,9 @@ enum {
   MOELORA_ERR_WORKSPACE = -4,     /* workspace null or smaller than required */
   MOELORA_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
   MOELORA_ERR_BAD_INDEX = -6,     /* device: topk_ids / lora_ids out of range */
-  MOELORA_ERR_TIMEOUT = -7        /* device: a bounded wait ran out */
+  MOELORA_ERR_TIMEOUT = -7,       /* device: a bounded wait ran out */
+  MOELORA_ERR_DEVICE_CHECK = -8   /* device, checked builds only: an internal index
+                                     failed its bounds check (the access was skipped) */
 };
 
 /* Sizes of one MoE-LoRA layer call.  T tokens, top-k, E experts, H hidden,

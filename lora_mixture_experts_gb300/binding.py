@@ -22,7 +22,7 @@ MOELORA_OK = 0
 STATUS = {
     0: "MOELORA_OK", -1: "MOELORA_ERR_INVALID_ARG", -2: "MOELORA_ERR_UNSUPPORTED",
     -3: "MOELORA_ERR_MISALIGNED", -4: "MOELORA_ERR_WORKSPACE", -5: "MOELORA_ERR_CUDA",
-    -6: "MOELORA_ERR_BAD_INDEX", -7: "MOELORA_ERR_TIMEOUT",
+    -6: "MOELORA_ERR_BAD_INDEX", -7: "MOELORA_ERR_TIMEOUT", -8: "MOELORA_ERR_DEVICE_CHECK",
 }
 
 
@@ -68,7 +68,9 @@ _SIGS = {
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library to load: libmoelora.so, or the file MOELORA_LIBRARY names
+    (the tests point it at the checked debug build)."""
+    return os.environ.get("MOELORA_LIBRARY") or _build.LIB
 
 
 def load(build_if_missing: bool = True):
@@ -78,6 +80,8 @@ def load(build_if_missing: bool = True):
         return _LIB
     path = library_path()
     if not os.path.exists(path):
+        if os.environ.get("MOELORA_LIBRARY"):
+            raise FileNotFoundError(f"MOELORA_LIBRARY={path} does not exist")
         if not build_if_missing:
             raise FileNotFoundError(f"{path} is not built; run lora_mixture_experts_gb300.build")
         _build.build()

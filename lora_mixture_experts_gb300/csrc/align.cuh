@@ -85,14 +85,16 @@ constexpr int kSmallMaxBins = 8192;
 bool align_small_fits(const AlignArgs& a);
 cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool chained, int num_sms);
 
-// x_perm[p] = x[row_tok[p]] (zero rows for padding), p < Pmax.
+// x_perm[p] = x[row_tok[p]] for rows with a token, p < Pmax (padding rows
+// are not written).  T and err serve the bounds checks of checked builds.
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
-                           int Pmax, int H, int num_sms, cudaStream_t stream);
+                           int Pmax, int H, int T, int* err, int num_sms, cudaStream_t stream);
 
 // out[t] = sum_j sum_s y_pair[s][pos_of[t*k+j]] in fp32 (j ascending, then
 // the K splits s in order), one bf16 rounding.  split_stride in floats.
+// Pmax and err serve the bounds checks of checked builds.
 cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
-                           int T, int k, int H, int nsplit, long long split_stride,
-                           int num_sms, cudaStream_t stream);
+                           int T, int k, int H, int nsplit, long long split_stride, int Pmax,
+                           int* err, int num_sms, cudaStream_t stream);
 
 }  // namespace moelora

@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
     const int pos = bin < 0 ? -1 : sm_bins[bin] + rank;
     if (gather) sm_pos[f] = pos;
     if (tables) {
-      if (bin < 0) {
+      if (bin < 0 || !MOELORA_IN_RANGE(&a.hdr->err, pos, 0, a.Pmax)) {
         if (a.pos_of) a.pos_of[f] = -1;
       } else {
         a.sorted_ids[pos] = f;
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kScanThreads) align_small_kernel(AlignArgs a) 
       const int fe = static_cast<int>(i / a.hv);
       const int u = static_cast<int>(i - static_cast<long long>(fe) * a.hv);
       const int pos = sm_pos[fe];
-      if (pos >= 0)
+      if (pos >= 0 && MOELORA_IN_RANGE(&a.hdr->err, pos, 0, a.Pmax))
         a.x_perm[static_cast<size_t>(pos) * a.hv + u] = a.x[static_cast<size_t>(fe / a.k) * a.hv + u];
     }
   }
@@ -421,6 +421,10 @@ __global__ void __launch_bounds__(kAlignChunk) align_scatter_kernel(AlignArgs a)
   }
   const int pos = a.bin_start[bin] + a.chunk_hist[static_cast<size_t>(c) * a.nbins + bin] +
                   a.rank_of[f];
+  if (!MOELORA_IN_RANGE(&a.hdr->err, pos, 0, a.Pmax)) {
+    if (a.pos_of) a.pos_of[f] = -1;
+    return;
+  }
   a.sorted_ids[pos] = f;
   if (a.row_tok) {
     a.row_tok[pos] = f / a.k;
@@ -440,7 +444,8 @@ constexpr int kPermUnroll = 4;
 
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ x,
                                                       const int* __restrict__ row_tok,
-                                                      uint4* __restrict__ x_perm, int Pmax, int hv) {
+                                                      uint4* __restrict__ x_perm, int Pmax, int hv,
+                                                      int T, int* err) {
   grid_dependency_wait();
   grid_dependency_trigger();
   const int lane = threadIdx.x & 31;
@@ -452,7 +457,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
     const int p = static_cast<int>(w / per_row);
     const int c0 = static_cast<int>(w - static_cast<long long>(p) * per_row) * 32 * kPermUnroll + lane;
     const int t = row_tok[p];
-    if (t < 0) continue;
+    if (t < 0 || !MOELORA_IN_RANGE(err, t, 0, T)) continue;
     const uint4* src = x + static_cast<size_t>(t) * hv;
     uint4* dst = x_perm + static_cast<size_t>(p) * hv;
     uint4 v[kPermUnroll];
@@ -481,7 +486,8 @@ template <int K, int NS>
 __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__ y_pair,
                                                       const int* __restrict__ pos_of,
                                                       uint2* __restrict__ out, int T, int kk,
-                                                      int nsplit, int hv, long long split_stride4) {
+                                                      int nsplit, int hv, long long split_stride4,
+                                                      int Pmax, int* err) {
   const int k = K > 0 ? K : kk;
   const int ns = NS > 0 ? NS : nsplit;
   const int lane = threadIdx.x & 31;
@@ -509,7 +515,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
     if (K > 0 && NS > 0) {
       int pos[K > 0 ? K : 1];
 #pragma unroll
-      for (int j = 0; j < K; ++j) pos[j] = w == w0 ? pos0[j] : pos_of[static_cast<size_t>(t) * K + j];
+      for (int j = 0; j < K; ++j) {
+        pos[j] = w == w0 ? pos0[j] : pos_of[static_cast<size_t>(t) * K + j];
+        if (pos[j] >= 0 && !MOELORA_IN_RANGE(err, pos[j], 0, Pmax)) pos[j] = -1;
+      }
       float4 v[K > 0 ? K : 1][NS > 0 ? NS : 1][kCombUnroll];
 #pragma unroll
       for (int j = 0; j < K; ++j)
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
     } else {
       for (int j = 0; j < k; ++j) {
         const int pos = pos_of[static_cast<size_t>(t) * k + j];
-        if (pos < 0) continue;
+        if (pos < 0 || !MOELORA_IN_RANGE(err, pos, 0, Pmax)) continue;
         for (int s = 0; s < ns; ++s)
 #pragma unroll
           for (int u = 0; u < kCombUnroll; ++u) {
@@ -612,7 +621,7 @@ cudaError_t launch_align_scatter(const AlignArgs& a, cudaStream_t stream, bool c
 }
 
 cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bfloat16* x_perm,
-                           int Pmax, int H, int num_sms, cudaStream_t stream) {
+                           int Pmax, int H, int T, int* err, int num_sms, cudaStream_t stream) {
   const int hv = H / 8;
   const long long items =
       static_cast<long long>(Pmax) * ((hv + 32 * kPermUnroll - 1) / (32 * kPermUnroll));
@@ -620,12 +629,12 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int* row_tok, __nv_bflo
   if (grid < 1) grid = 1;
   return launch_chained(permute_kernel, dim3(grid), dim3(256), 0, stream, true,
                         reinterpret_cast<const uint4*>(x), row_tok, reinterpret_cast<uint4*>(x_perm),
-                        Pmax, hv);
+                        Pmax, hv, T, err);
 }
 
 cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16* out,
-                           int T, int k, int H, int nsplit, long long split_stride,
-                           int num_sms, cudaStream_t stream) {
+                           int T, int k, int H, int nsplit, long long split_stride, int Pmax,
+                           int* err, int num_sms, cudaStream_t stream) {
   const int hv = H / 4;
   const long long items =
       static_cast<long long>(T) * ((hv + 32 * kCombUnroll - 1) / (32 * kCombUnroll));
@@ -634,7 +643,7 @@ cudaError_t launch_combine(const float* y_pair, const int* pos_of, __nv_bfloat16
   auto go = [&](auto kernel) {
     return launch_chained(kernel, dim3(grid), dim3(128), 0, stream, true,
                           reinterpret_cast<const float4*>(y_pair), pos_of, reinterpret_cast<uint2*>(out), T,
-                          k, nsplit, hv, split_stride / 4);
+                          k, nsplit, hv, split_stride / 4, Pmax, err);
   };
   if (nsplit == 1) {
     if (k == 1) return go(combine_kernel<1, 1>);

@@ -47,10 +47,26 @@ struct WsHeader {
 
 constexpr int kStatusBadIndex = MOELORA_ERR_BAD_INDEX;
 constexpr int kStatusTimeout = MOELORA_ERR_TIMEOUT;
+constexpr int kStatusDeviceCheck = MOELORA_ERR_DEVICE_CHECK;
 
 __device__ __forceinline__ void flag_error(int* err, int code) {
   atomicCAS(err, 0, code);
 }
+
+// Device-side bounds checks of indices the kernels take from the align's
+// tables (debug builds compiled with -DMOELORA_DEVICE_CHECKS): a failing
+// index flags MOELORA_ERR_DEVICE_CHECK and the access it guards is skipped,
+// never trapped.  Release builds compile every check to `true`.
+__device__ __forceinline__ bool device_check(int* err, bool ok) {
+  if (!ok) flag_error(err, kStatusDeviceCheck);
+  return ok;
+}
+#ifdef MOELORA_DEVICE_CHECKS
+#define MOELORA_IN_RANGE(err, v, lo, hi) \
+  ::moelora::device_check((err), (v) >= (lo) && (v) < (hi))
+#else
+#define MOELORA_IN_RANGE(err, v, lo, hi) true
+#endif
 
 // ---------------------------------------------------------------- launch chaining
 // Programmatic dependent launch: every kernel of the layer waits for the

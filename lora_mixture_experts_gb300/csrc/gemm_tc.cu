@@ -439,7 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cp = (i0 + j) - sl * per_slot;
                 const int c = cp / p.z_parts;
                 const int part = cp - c * p.z_parts;
-                const int a = p.slot_adapter[ti.slot_base + sl];
+                // (a failed check loads slot 0's data instead: the stage still
+                // receives the bytes its barrier expects)
+                const int sidx_ok =
+                    MOELORA_IN_RANGE(p.err, ti.slot_base + sl, 0, p.zpart_slots) ? ti.slot_base + sl : 0;
+                const int a = p.slot_adapter[sidx_ok];
                 if (gate_up)
                   load5(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, 0, grow, ti.expert, a);
                 else
@@ -656,7 +660,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ShrinkItem si = p.shrink[it.sh];
         const int j = static_cast<int>(rank) * spc + row / p.r;   // slot of the item
         const int q = row % p.r;
-        const bool valid = j < si.nslot && row / p.r < spc;
+        const bool valid = j < si.nslot && row / p.r < spc &&
+                           MOELORA_IN_RANGE(p.err, si.slot0 + j, 0, p.zpart_slots) &&
+                           MOELORA_IN_RANGE(p.err, ti.expert, 0, p.n_experts);
         const int a_j = valid ? p.slot_adapter[si.slot0 + j] : -3;
         __nv_bfloat16* zrow =
             p.zbuf + (static_cast<size_t>(si.slot0 + (valid ? j : 0)) * TN) * (p.z_parts * p.r) + q;
@@ -758,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float g = is_gate ? v[cc] : other;
             const float u = is_gate ? other : v[half + cc];
             const int c = cbase + cc;
-            if (store_ok && c < ti.nrows)
+            if (store_ok && c < ti.nrows && MOELORA_IN_RANGE(p.err, ti.row0 + c, 0, p.Pmax))
               orow[static_cast<size_t>(c) * p.out_ld] = __float2bfloat16_rn(silu_f(g) * u);
           }
         };
@@ -785,9 +791,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = c0 + cc;
               if (c < ti.nrows) {
                 const int prow = ti.row0 + c;
+                if (!MOELORA_IN_RANGE(p.err, prow, 0, p.Pmax)) continue;
                 if (linear) {
-                  p.out[static_cast<size_t>(p.row_tok[prow]) * p.out_ld + feat] =
-                      __float2bfloat16_rn(v[cc]);
+                  const int t = p.row_tok[prow];
+                  if (MOELORA_IN_RANGE(p.err, t, 0, p.T))
+                    p.out[static_cast<size_t>(t) * p.out_ld + feat] = __float2bfloat16_rn(v[cc]);
                 } else {
                   p.out_f32[it.ks * p.split_stride + static_cast<size_t>(prow) * p.out_ld + feat] =
                       v[cc] * p.row_w[prow];

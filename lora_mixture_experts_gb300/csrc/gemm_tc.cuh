@@ -53,6 +53,10 @@ struct GemmParams {
   // sums the parts in split order and writes zbuf.
   int sh_splits;
   float* zpart;
+  // sizes for the device-side bounds checks of checked builds
+  int Pmax;               // sorted-row capacity
+  int T;                  // tokens
+  int n_experts;
   int zpart_slots;
   int* sh_cnt;
   // Shrink results [slots * tn][z_parts * r].  z_parts = 2 keeps each as two

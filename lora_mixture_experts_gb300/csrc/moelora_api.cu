@@ -698,6 +698,9 @@ GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   g.row_w = a.row_w;
   g.row_tok = a.row_tok;
   g.tile_done = a.tile_done;
+  g.Pmax = p.Pmax;
+  g.T = p.T;
+  g.n_experts = p.E;
   g.sh_splits = p.sks;
   g.zpart = p.sks > 1 ? ws_ptr<float>(ws, p.off_zpart) : nullptr;
   g.zpart_slots = p.n_slots_max;
@@ -901,7 +904,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   if (!gathered) {
     ln.before("permute");
     MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
-                                      p.Pmax, p.H, sms, stream));
+                                      p.Pmax, p.H, p.T, &a.hdr->err, sms, stream));
   }
   ln.before("gemm_gate_up");
   MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles, sms), stream));
@@ -909,8 +912,8 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles * p.ksplit, sms), stream));
   ln.before("combine");
   MOELORA_CUDA_CHECK(launch_combine(ypair, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
-                                    p.k, p.H, p.ksplit, static_cast<long long>(p.Pmax) * p.H, sms,
-                                    stream));
+                                    p.k, p.H, p.ksplit, static_cast<long long>(p.Pmax) * p.H, p.Pmax,
+                                    &a.hdr->err, sms, stream));
   ln.finish();
   return MOELORA_OK;
 }
@@ -1028,15 +1031,15 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   if (!gathered) {
     ln.before("permute");
     MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
-                                      p.Pmax, p.H, sms, stream));
+                                      p.Pmax, p.H, p.T, &a.hdr->err, sms, stream));
   }
   ln.before("gemm_linear");
   MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, m, g, gemm_grid(p, g.n_mtiles * p.ksplit, sms), stream));
   if (p.ksplit > 1) {
     ln.before("combine");
     MOELORA_CUDA_CHECK(launch_combine(partial, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
-                                      1, p.N, p.ksplit, static_cast<long long>(p.Pmax) * p.N, sms,
-                                      stream));
+                                      1, p.N, p.ksplit, static_cast<long long>(p.Pmax) * p.N, p.Pmax,
+                                      &a.hdr->err, sms, stream));
   }
   ln.finish();
   return MOELORA_OK;
@@ -1145,6 +1148,7 @@ const char* moelora_status_string(int s) {
     case MOELORA_ERR_CUDA: return "CUDA error";
     case MOELORA_ERR_BAD_INDEX: return "expert or adapter id out of range";
     case MOELORA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case MOELORA_ERR_DEVICE_CHECK: return "a device-side bounds check failed (checked build)";
     default: return "unknown status";
   }
 }

@@ -35,7 +35,7 @@ int main(void) {
                           fake, fake, ws, NULL) == MOELORA_ERR_INVALID_ARG, "null x");
   expect(moe_lora_forward(&decode, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                           fake, fake, ws - 1, NULL) == MOELORA_ERR_WORKSPACE, "workspace too small");
-  for (int s = MOELORA_OK; s >= MOELORA_ERR_TIMEOUT; --s)
+  for (int s = MOELORA_OK; s >= MOELORA_ERR_DEVICE_CHECK; --s)
     expect(moelora_status_string(s) != NULL && moelora_status_string(s)[0] != '\0', "status string");
   printf("%s %zu\n", fails ? "FAILED" : "OK", ws);
   return fails != 0;
