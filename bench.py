@@ -189,13 +189,13 @@ def oracle_baseline(case, host, seconds, tokens=None):
     t0 = time.perf_counter()
     while True:
         if isinstance(case, LinearCase):
-            ref.moe_lora_linear_ref(host["x"][tokens], host["lora_ids"][tokens], host["W"],
-                                    host["A"], host["B"])
+            y = ref.moe_lora_linear_ref(host["x"][tokens], host["lora_ids"][tokens], host["W"],
+                                        host["A"], host["B"])
         else:
-            ref.moe_lora_forward_ref(host["x"], host["topk_ids"], host["topk_weights"],
-                                     host["lora_ids"], host["W_gate_up"], host["W_down"],
-                                     host.get("A_gu"), host.get("B_gu"), host.get("A_d"),
-                                     host.get("B_d"), tokens=tokens)
+            y = ref.moe_lora_forward_ref(host["x"], host["topk_ids"], host["topk_weights"],
+                                         host["lora_ids"], host["W_gate_up"], host["W_down"],
+                                         host.get("A_gu"), host.get("B_gu"), host.get("A_d"),
+                                         host.get("B_d"), tokens=tokens)
         n_done += len(tokens)
         reps += 1
         el = time.perf_counter() - t0
@@ -203,7 +203,22 @@ def oracle_baseline(case, host, seconds, tokens=None):
             break
     sample = (f"{len(tokens)} of {T} tokens of the {case.name} batch per oracle call, "
               f"{reps} calls in {el:.1f} s")
-    return n_done / el, sample
+    return n_done / el, sample, y
+
+
+def parity_summary(gpu_rows, ref_rows):
+    """The layer's acceptance figures for the timed output against the
+    oracle's rows of the same tokens: relative Frobenius error (tolerance
+    1e-2) and max-abs error over the oracle's RMS (tolerance 3e-2)."""
+    import numpy as np
+    g = gpu_rows.float().cpu().numpy().astype(np.float64)
+    d = g - ref_rows
+    rel = float(np.linalg.norm(d) / max(np.linalg.norm(ref_rows), 1e-30))
+    rms = float(np.sqrt(np.mean(ref_rows ** 2)))
+    mx = float(np.abs(d).max() / max(rms, 1e-30))
+    return {"tokens": int(ref_rows.shape[0]), "rel_fro": rel, "max_abs_over_rms": mx,
+            "tolerance": {"rel_fro": 1e-2, "max_abs_over_rms": 3e-2},
+            "pass": bool(np.all(np.isfinite(g)) and rel <= 1e-2 and mx <= 3e-2)}
 
 
 def host_inputs(d):
@@ -446,9 +461,11 @@ def run_ours(args, rank, world, device):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         hostw = host_inputs({k: v for k, v in d.items()})
         tokens = sample_tokens(case, oracle_budget_tokens(case))
-        v, sample = oracle_baseline(case, hostw, args.cpu_seconds, tokens)
+        v, sample, y = oracle_baseline(case, hostw, args.cpu_seconds, tokens)
         res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                                "sample": sample}
+        # the timed calls' output against the oracle's rows of the sampled tokens
+        res["parity"] = parity_summary(out[torch.as_tensor(tokens, device=out.device)], y)
     return res
 
 
