@@ -317,7 +317,9 @@ def run_ours(args, rank, world, device):
                                      d["A_d"], d["B_d"], out=out, ws=ws)
         layer, gu, dn = roofline.moe_layer_work(d["topk_ids"].cpu().numpy(), d["lora_ids"].cpu().numpy(),
                                                 case.H, case.I, case.r)
-        kernel_work = {"gemm_gate_up": gu, "gemm_down": dn}
+        # single-CTA tiles run both projections in one launch
+        kernel_work = {"gemm_gate_up": gu, "gemm_down": dn,
+                       "gemm_gate_up_down": roofline.Work(gu.bytes + dn.bytes, gu.flops + dn.flops)}
         step_inputs = ["x", "topk_ids", "topk_weights", "lora_ids"]
 
     stream = torch.cuda.current_stream()

@@ -53,6 +53,7 @@ struct AlignArgs {
   int* sh_cnt;                  // [2 * shrink items] split arrivals per item and CTA of a pair
   int* slot_adapter;
   int* tile_done;
+  int* act_done;                // [tiles] gate_up items done per tile (two-phase launch), or NULL
   // 1: the single-CTA align zeroes the workspace error word before anything
   // can flag it (the call then needs no separate memset)
   int reset_err;

@@ -273,6 +273,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
       }
       a.tiles[tbase + j] = ti;
       a.tile_done[tbase + j] = 0;
+      if (a.act_done) a.act_done[tbase + j] = 0;
       sl += ns;
       sh += nh;
     }

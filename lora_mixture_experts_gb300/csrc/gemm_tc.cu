@@ -167,10 +167,22 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-template <int TN, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+// One launch runs one phase (n_phases = 1: maps0 / p0), or on single-CTA
+// tiles both phases of the layer (n_phases = 2: gate_up items, then down
+// items, one item order and one claim counter).  A down item then waits for
+// its token tile's activation rows: every gate_up main item of the tile
+// counts on act_done[tile] once its rows are stored.  Items are claimed in
+// order and every CTA is resident, so the wait ends.
+// The body of both kernels below.  NPH is a template argument so that the
+// one-phase kernel reads its parameters at fixed offsets (no per-item
+// selection between p0 and p1: maps1 / p1 alias maps0 / p0 there).
+template <int TN, bool PAIR, int NPH>
+__device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps& maps1,
+                                          const GemmParams& p0, const GemmParams& p1) {
+  constexpr int n_phases = NPH;
   using C = Cfg<TN, PAIR>;
+  // fields shared by the phases (tables, counters, sizes) are read from p0
+  const GemmParams& p = p0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -215,11 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&maps.w);
-    if (p.r > 0) {
-      tma_prefetch_desc(&maps.lb);
-      tma_prefetch_desc(&maps.la);
-      tma_prefetch_desc(&maps.la_run);
+    for (int ph = 0; ph < n_phases; ++ph) {
+      const GemmMaps& mp = NPH == 2 && ph ? maps1 : maps0;
+      tma_prefetch_desc(&mp.w);
+      if (p.r > 0) {
+        tma_prefetch_desc(&mp.lb);
+        tma_prefetch_desc(&mp.la);
+        tma_prefetch_desc(&mp.la_run);
+      }
     }
   }
   if (warp == 1) {
@@ -246,9 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tiles = p.hdr->n_tiles;
   const int n_sh = p.r > 0 ? p.hdr->n_shrink : 0;
-  const int n_items = n_sh + n_tiles * p.n_mtiles * p.ksplit;
-  const int nk = (p.K + 63) / 64;             // 64-wide K chunks of the base GEMM
-  const bool gate_up = p.mode == kModeGateUp;
+  const int items0 = n_sh + n_tiles * p0.n_mtiles * p0.ksplit;
+  const int n_items = items0 + (n_phases > 1 ? n_sh + n_tiles * p1.n_mtiles * p1.ksplit : 0);
   const int spc = p.r > 0 ? 128 / p.r : 0;    // shrink slots per CTA
   // shrink completions a tile's item waits for: every CTA of the item signals
   const int done_scale = PAIR ? 2 : 1;
@@ -285,25 +299,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int v) {
         if (PAIR) tma_load_5d_pair(dst, m, fb, x, y, z, w, v); else tma_load_5d(dst, m, fb, x, y, z, w, v);
       };
-      // Before the grid dependency wait (first item only, unpaired tiles),
-      // a stage gets its weight blocks and its barrier's byte count; the
-      // token rows of those stages (slots 0 .. n_def-1, K chunk i of the item
-      // = kc0 + i rotated by rot within nkc) are loaded after the wait, which
-      // comes once the ring is full or the item's K loop ends.
+      // Deferred token rows.  Before the grid dependency wait (first item,
+      // unpaired tiles), or before its tile's activations are complete (a
+      // down item of the two-phase launch), a stage gets its weight blocks
+      // and its barrier's byte count; the token rows of those stages (the
+      // n_def ring slots from def_s0 on, K chunk i of the item = kc0 + i
+      // rotated by rot within nkc) are loaded after the wait, which comes
+      // once the ring is full or the item's K loop ends.
       bool waited = !early;
       int n_def = 0;
-      auto load_deferred_rows = [&](int nkc, int kc0, int rot, const CUtensorMap* tb, int brow0) {
-        grid_dependency_wait();
-        for (int d = 0; d < n_def; ++d) {
-          const uint32_t st = smem_u32(smem + d * C::kStageBytes);
-          const uint32_t fb = smem_u32(&full_bar[d]);
-          for (int j = 0; j < C::kKB && d * C::kKB + j < nkc; ++j) {
-            const int i = d * C::kKB + j;
-            const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
-            load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+      int def_s0 = 0;
+      const int* defer_cnt = nullptr;   // NULL: wait for the preceding launch
+      int defer_target = 0;
+      bool defer_ok = true;
+      auto load_deferred_rows = [&](int nkc, int kc0, int rot, const CUtensorMap* tb,
+                                    int brow0) -> bool {
+        if (defer_cnt) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(defer_cnt) < defer_target) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+              defer_ok = false;
+              break;
+            }
+            __nanosleep(64);
+          }
+          fence_proxy_async_global();
+          defer_cnt = nullptr;
+        } else {
+          grid_dependency_wait();
+        }
+        if (defer_ok) {
+          for (int d = 0; d < n_def; ++d) {
+            const int s = def_s0 + d < C::kStages ? def_s0 + d : def_s0 + d - C::kStages;
+            const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+            const uint32_t fb = smem_u32(&full_bar[s]);
+            for (int j = 0; j < C::kKB && d * C::kKB + j < nkc; ++j) {
+              const int i = d * C::kKB + j;
+              const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
+              load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+            }
           }
         }
         waited = true;
+        return defer_ok;
       };
       // stage s of this CTA is free: wait on its empty barrier; the barrier
       // that counts the stage's bytes is the leader's full barrier
@@ -329,7 +367,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileInfo ti;
         if (!(ok = ring_take(qc, w, ti, true))) break;
         if (w < 0) break;
-        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+        const int ph = NPH == 2 && w >= items0 ? 1 : 0;
+        const GemmParams& p = NPH == 2 && ph ? p1 : p0;
+        const GemmMaps& maps = NPH == 2 && ph ? maps1 : maps0;
+        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
+                                    p.shrink);
+        const int nk = (p.K + 63) / 64;             // 64-wide K chunks of the base GEMM
+        const bool gate_up = p.mode == kModeGateUp;
+        if (p.act_wait) {
+          // a down item of the two-phase launch: its token rows are the
+          // tile's activations, complete once every gate_up item of the tile
+          // has counted.  Ready: make them visible to TMA.  Not yet: stream
+          // the item's weight blocks and defer its token rows to the wait.
+          if (ld_acquire_gpu(&p.act_wait[it.tile]) >= p.act_target) {
+            fence_proxy_async_global();
+          } else {
+            waited = false;
+            n_def = 0;
+            def_s0 = sidx;
+            defer_cnt = &p.act_wait[it.tile];
+            defer_target = p.act_target;
+          }
+        }
         const int nmma = (ti.nrows + 15) & ~15;
         const int nh = PAIR ? nmma / 2 : nmma;          // token rows this CTA loads
         const int bi = box_index(nh);
@@ -373,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
-            if (!waited && ++n_def == C::kStages)
-              load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0);
+            if (!waited && ++n_def == C::kStages && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0))
+              ok = false;
           }
-          if (!waited) load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0);
+          if (ok && !waited && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0)) ok = false;
         } else {
           const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
           const int kc0 = p.split_k0[it.ks];
@@ -404,9 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load3(st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
               if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
-            if (!waited && ++n_def == C::kStages) load_deferred_rows(nkc, kc0, rot, tb, brow0);
+            if (!waited && ++n_def == C::kStages && !load_deferred_rows(nkc, kc0, rot, tb, brow0))
+              ok = false;
           }
-          if (!waited) load_deferred_rows(nkc, kc0, rot, tb, brow0);
+          if (ok && !waited && !load_deferred_rows(nkc, kc0, rot, tb, brow0)) ok = false;
           if (ok && p.r > 0 && ti.nslots > 0 && it.ks == p.ksplit - 1) {
             // the tile's shrink results must be complete and visible to TMA
             const int target = p.done_target * ti.nsh * done_scale;
@@ -487,7 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileInfo ti;
         if (!(ok = ring_take(qc, w, ti, false))) break;
         if (w < 0) break;
-        const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+        const int ph = NPH == 2 && w >= items0 ? 1 : 0;
+        const GemmParams& p = NPH == 2 && ph ? p1 : p0;
+        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
+                                    p.shrink);
+        const int nk = (p.K + 63) / 64;
         const int nmma = (ti.nrows + 15) & ~15;
         const uint32_t idesc = make_idesc_bf16(nmma, PAIR ? 256 : 128);
         const int buf = li & 1;
@@ -612,7 +676,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int w = dyn ? atomicAdd(p.work_ctr, 1) : unit + static_cast<int>(qp) * n_units;
         if (w >= n_items) w = -1;
-        if (w >= 0) ring[q].ti = p.tiles[decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink).tile];
+        if (w >= 0) {
+          const bool w1 = NPH == 2 && w >= items0;
+          const GemmParams& pw = w1 ? p1 : p0;
+          ring[q].ti = p.tiles[decode_item(w - (w1 ? items0 : 0), n_sh, n_tiles, pw.n_mtiles,
+                                           pw.group_tiles, p.shrink).tile];
+        }
         ring[q].w = w;
         mbar_arrive(smem_u32(&itemf_bar[q]));
         if (w < 0) break;
@@ -644,7 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&iteme_bar[q]));
       if (w < 0) break;
-      const Item it = decode_item(w, n_sh, n_tiles, p.n_mtiles, p.group_tiles, p.shrink);
+      const int ph = NPH == 2 && w >= items0 ? 1 : 0;
+      const GemmParams& p = NPH == 2 && ph ? p1 : p0;
+      const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
+                                  p.shrink);
+      const bool gate_up = p.mode == kModeGateUp;
       const int nmma = (ti.nrows + 15) & ~15;
       const int buf = li & 1;
       const bool ok = mbar_wait(smem_u32(&accf_bar[buf]), (li >> 1) & 1, abort_flag);
@@ -779,6 +852,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(t_row + c0, v);
           finish(v, c0, 8);
         }
+        if (p.act_count) {
+          // two-phase launch: publish this item's activation rows to the
+          // tile's down items (every thread's stores, then one release)
+          named_bar_sync(1, 128);
+          if (row == 0) {
+            __threadfence();
+            fence_proxy_async_global();
+            atomicAdd(&p.act_count[it.tile], 1);
+          }
+        }
       } else {
         const int feat = it.m * C::kMRows + static_cast<int>(rank) * 128 + row;
         const bool linear = p.mode == kModeLinear;
@@ -827,8 +910,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One phase per launch: the parameters by value, read at fixed offsets.
 template <int TN, bool PAIR>
-cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  gemm_body<TN, PAIR, 1>(maps, maps, p, p);
+}
+
+// Both phases in one launch (single-CTA tiles): the items pick their phase's
+// maps and parameters, so these are grid constants (addressable in place).
+template <int TN>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_two_phase_kernel(const __grid_constant__ GemmMaps maps0,
+                              const __grid_constant__ GemmMaps maps1,
+                              const __grid_constant__ GemmParams p0,
+                              const __grid_constant__ GemmParams p1) {
+  gemm_body<TN, false, 2>(maps0, maps1, p0, p1);
+}
+
+template <int TN, bool PAIR, int NPH>
+struct KernelOf {
+  static constexpr auto fn = moe_gemm_kernel<TN, PAIR>;
+};
+template <int TN>
+struct KernelOf<TN, false, 2> {
+  static constexpr auto fn = moe_gemm_two_phase_kernel<TN>;
+};
+
+template <int TN, bool PAIR, int NPH>
+cudaError_t launch_tn(const GemmMaps& maps0, const GemmParams& p0, const GemmMaps& maps1,
+                      const GemmParams& p1, int grid, cudaStream_t stream) {
   using C = Cfg<TN, PAIR>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static int configured_device = -1;
@@ -836,7 +947,7 @@ cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaS
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<TN, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(KernelOf<TN, PAIR, NPH>::fn,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -853,12 +964,12 @@ cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaS
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<TN, PAIR>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&clusters, KernelOf<TN, PAIR, NPH>::fn, &cfg);
       if (e != cudaSuccess) return e;
       max_units = clusters;
     } else {
       int per_sm = 0, sms = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_gemm_kernel<TN, PAIR>, kThreads,
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KernelOf<TN, PAIR, NPH>::fn, kThreads,
                                                         C::kSmemBytes);
       if (e != cudaSuccess) return e;
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -887,7 +998,10 @@ cudaError_t launch_tn(const GemmMaps& maps, const GemmParams& p, int grid, cudaS
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<TN, PAIR>, maps, p);
+  if constexpr (NPH == 2)
+    return cudaLaunchKernelEx(&cfg, KernelOf<TN, PAIR, NPH>::fn, maps0, maps1, p0, p1);
+  else
+    return cudaLaunchKernelEx(&cfg, KernelOf<TN, PAIR, NPH>::fn, maps0, p0);
 }
 
 }  // namespace
@@ -911,11 +1025,21 @@ int moe_gemm_stage_kblocks(int tn) {
 
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream) {
-  if (tn == 256) return launch_tn<256, true>(maps, p, grid, stream);
-  if (tn == 128) return launch_tn<128, false>(maps, p, grid, stream);
-  if (tn == 64) return launch_tn<64, false>(maps, p, grid, stream);
-  if (tn == 32) return launch_tn<32, false>(maps, p, grid, stream);
-  if (tn == 16) return launch_tn<16, false>(maps, p, grid, stream);
+  if (tn == 256) return launch_tn<256, true, 1>(maps, p, maps, p, grid, stream);
+  if (tn == 128) return launch_tn<128, false, 1>(maps, p, maps, p, grid, stream);
+  if (tn == 64) return launch_tn<64, false, 1>(maps, p, maps, p, grid, stream);
+  if (tn == 32) return launch_tn<32, false, 1>(maps, p, maps, p, grid, stream);
+  if (tn == 16) return launch_tn<16, false, 1>(maps, p, maps, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_moe_gemm_two_phase(int tn, const GemmMaps& maps0, const GemmParams& p0,
+                                      const GemmMaps& maps1, const GemmParams& p1, int grid,
+                                      cudaStream_t stream) {
+  if (tn == 128) return launch_tn<128, false, 2>(maps0, p0, maps1, p1, grid, stream);
+  if (tn == 64) return launch_tn<64, false, 2>(maps0, p0, maps1, p1, grid, stream);
+  if (tn == 32) return launch_tn<32, false, 2>(maps0, p0, maps1, p1, grid, stream);
+  if (tn == 16) return launch_tn<16, false, 2>(maps0, p0, maps1, p1, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -53,6 +53,13 @@ struct GemmParams {
   // sums the parts in split order and writes zbuf.
   int sh_splits;
   float* zpart;
+  // Two-phase launch (gate_up then down in one persistent launch): the
+  // gate_up phase counts each finished item on act_count[tile]; a down item
+  // waits until act_wait[tile] reaches act_target (the tile's gate_up items).
+  // Both NULL in a one-phase launch.
+  int* act_count;
+  const int* act_wait;
+  int act_target;
   // sizes for the device-side bounds checks of checked builds
   int Pmax;               // sorted-row capacity
   int T;                  // tokens
@@ -81,6 +88,13 @@ struct GemmParams {
 // 128 or 256.
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream);
+
+// Both phases of the layer in one persistent launch (single-CTA tiles only,
+// tn < 256): the gate_up items (maps0 / p0, p0.act_count set), then the down
+// items (maps1 / p1, p1.act_wait and act_target set).
+cudaError_t launch_moe_gemm_two_phase(int tn, const GemmMaps& maps0, const GemmParams& p0,
+                                      const GemmMaps& maps1, const GemmParams& p1, int grid,
+                                      cudaStream_t stream);
 
 // Dynamic shared memory of the kernel for a token-tile width.
 size_t moe_gemm_smem_bytes(int tn);

@@ -45,7 +45,7 @@ struct Plan {
   size_t off_sorted = 0, off_blk = 0, off_seg = 0;
   size_t off_row_tok = 0, off_row_lora = 0, off_row_w = 0, off_pos_of = 0;
   size_t off_tiles = 0, off_shrink = 0, off_slot_ad = 0, off_tile_done = 0;
-  size_t off_sh_cnt = 0, off_zpart = 0;
+  size_t off_sh_cnt = 0, off_zpart = 0, off_act_done = 0;
   size_t off_xperm = 0, off_zgu = 0, off_zd = 0, off_act = 0, off_ypair = 0;
   size_t off_topk_ids = 0, off_topk_w = 0;   // router results (routed forward)
   size_t total = 0;
@@ -86,13 +86,14 @@ int first_phase_done_target() {
 // Lines of `key=value` tokens, '#' starts a comment.  The first token is the
 // entry kind (`moe` or `linear`); shape keys T (a value or a range lo-hi),
 // k, E, H, I, K, N, L, r must match when present (absent = any); the choice
-// keys tn (16/32/64/128/256) and ksplit (1..4) override the built-in
-// choice.  The first matching line wins.
+// keys tn (16/32/64/128/256), ksplit (1..4) and phases (1 = one launch per
+// projection, 2 = both projections in one launch on single-CTA tiles)
+// override the built-in choice.  The first matching line wins.
 struct TuneEntry {
   bool linear = false;
   int t_lo = 0, t_hi = 0x7fffffff;
   int k = -1, E = -1, H = -1, I = -1, L = -1, r = -1;   // H = K, I = N for linear
-  int tn = 0, ksplit = 0;
+  int tn = 0, ksplit = 0, phases = 0;
 };
 
 std::mutex g_tune_mu;
@@ -142,6 +143,9 @@ bool parse_tune_line(const std::string& line, TuneEntry& e, bool& is_entry) {
     } else if (key == "ksplit") {
       if (iv < 1 || iv > 4) return false;
       e.ksplit = iv;
+    } else if (key == "phases") {
+      if (iv < 1 || iv > 2) return false;
+      e.phases = iv;
     } else {
       return false;
     }
@@ -163,7 +167,8 @@ int load_tune_file(const std::string& path, std::vector<TuneEntry>& out) {
 }
 
 // Choice for a shape from the loaded table (tn, ksplit; 0 = no override).
-void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, int& tn, int& ks) {
+void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, int& tn, int& ks,
+                 int* phases = nullptr) {
   std::lock_guard<std::mutex> lk(g_tune_mu);
   for (const TuneEntry& e : g_tune) {
     if (e.linear != linear || T < e.t_lo || T > e.t_hi) continue;
@@ -172,6 +177,7 @@ void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, i
       continue;
     if (e.tn) tn = e.tn;
     if (e.ksplit) ks = e.ksplit;
+    if (phases && e.phases) *phases = e.phases;
     return;
   }
 }
@@ -278,6 +284,7 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   p.off_sh_cnt = b.take(static_cast<size_t>(std::max(p.n_sh_max, 1)) * 2 * 4);
   p.off_slot_ad = b.take(static_cast<size_t>(std::max(p.n_slots_max, 1)) * 4);
   p.off_tile_done = b.take(static_cast<size_t>(p.n_tiles_max) * 4);
+  p.off_act_done = b.take(static_cast<size_t>(p.n_tiles_max) * 4);
   p.off_xperm = b.take(static_cast<size_t>(p.Pmax) * p.H * 2);
   // gate_up shrink results: per slot and token row, hi and lo bf16 rows of r
   // (the dense linear uses the first half only)
@@ -892,6 +899,28 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   // decode 249.0 -> 246.4 us; on the gate_up and dense-linear launches, whose
   // predecessor is the short permute, the deferred first token rows cost more)
   gd.early_weights = 1;
+  // Single-CTA tiles of a layer with several experts run both phases in
+  // one persistent launch: a CTA that runs out of gate_up items goes on to
+  // down items of tiles whose activations are complete, instead of idling
+  // until the last gate_up item of the launch ends (decode 242.8 -> 239.0
+  // us).  With one expert every down item waits for all of gate_up, and two
+  // launches were as fast or faster (E = 1, T = 8: 146.0 against 152.3 us;
+  // T = 64: 200.3 against 191.5, so the tuned table picks per workload).
+  // The table's `phases` key or MOELORA_TWO_PHASE (0 / 1) override this.
+  int phases = p.E > 1 ? 2 : 1;
+  {
+    int t_tn = 0, t_ks = 0;
+    tune_lookup(false, p.T, p.k, p.E, p.H, p.I, p.L, p.r, t_tn, t_ks, &phases);
+  }
+  if (const char* tp = std::getenv("MOELORA_TWO_PHASE")) phases = std::strcmp(tp, "0") == 0 ? 1 : 2;
+  const bool two_phase = !paired && phases == 2;
+  if (two_phase) {
+    int* act_done = ws_ptr<int>(ws, p.off_act_done);
+    a.act_done = act_done;          // zeroed by the align
+    gu.act_count = act_done;
+    gd.act_wait = act_done;
+    gd.act_target = gu.n_mtiles * gu.ksplit;
+  }
 
   Launcher ln(stream);
   if (!routed) {   // the small-batch align gathers the token rows itself
@@ -906,10 +935,16 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
     MOELORA_CUDA_CHECK(launch_permute(reinterpret_cast<const __nv_bfloat16*>(x), a.row_tok, x_perm,
                                       p.Pmax, p.H, p.T, &a.hdr->err, sms, stream));
   }
-  ln.before("gemm_gate_up");
-  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles, sms), stream));
-  ln.before("gemm_down");
-  MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles * p.ksplit, sms), stream));
+  if (two_phase) {
+    ln.before("gemm_gate_up_down");
+    MOELORA_CUDA_CHECK(launch_moe_gemm_two_phase(
+        p.tn, mg, gu, md, gd, gemm_grid(p, gu.n_mtiles + gd.n_mtiles * p.ksplit, sms), stream));
+  } else {
+    ln.before("gemm_gate_up");
+    MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles, sms), stream));
+    ln.before("gemm_down");
+    MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles * p.ksplit, sms), stream));
+  }
   ln.before("combine");
   MOELORA_CUDA_CHECK(launch_combine(ypair, a.pos_of, reinterpret_cast<__nv_bfloat16*>(out), p.T,
                                     p.k, p.H, p.ksplit, static_cast<long long>(p.Pmax) * p.H, p.Pmax,

@@ -3,7 +3,8 @@ and writes a tuning table for ``moelora_load_tuning``.
 
     python -m lora_mixture_experts_gb300.tune [--out FILE] [--configs decode,prefill,...]
 
-For every workload and every candidate (token tile tn, K split) it forces the
+For every workload and every candidate (token tile tn, K split, and on
+single-CTA tiles one or two launches for the projections) it forces the
 candidate with a one-line table, times the whole layer call with CUDA events
 and keeps the fastest; the table lines match the workload's exact shape.
 (The multi-LoRA MoE blog tunes its kernels' block sizes and split factors per
@@ -81,22 +82,26 @@ def sweep(names, out_path, device="cuda", log=print):
             default_ms = _time(make())
             best = None
             for tn in TILES:
+                # both projections in one launch is an option on single-CTA tiles
+                phase_opts = (1, 2) if (not isinstance(case, LinearCase) and tn < 256) else (0,)
                 for ks in (1, 2, 3, 4):
-                    with open(cand_file, "w") as f:
-                        f.write(f"{_shape_line(case)} tn={tn} ksplit={ks}\n")
-                    binding.moelora_load_tuning(cand_file)
-                    ms = _time(make())
-                    log(f"{name}: tn={tn} ksplit={ks}: {ms:.4f} ms")
-                    if best is None or ms < best[0]:
-                        best = (ms, tn, ks)
+                    for ph in phase_opts:
+                        extra = f" phases={ph}" if ph else ""
+                        with open(cand_file, "w") as f:
+                            f.write(f"{_shape_line(case)} tn={tn} ksplit={ks}{extra}\n")
+                        binding.moelora_load_tuning(cand_file)
+                        ms = _time(make())
+                        log(f"{name}: tn={tn} ksplit={ks}{extra}: {ms:.4f} ms")
+                        if best is None or ms < best[0]:
+                            best = (ms, tn, ks, extra)
             binding.moelora_load_tuning(None)
-            ms, tn, ks = best
+            ms, tn, ks, extra = best
             if ms < (1.0 - KEEP_MARGIN) * default_ms:
-                lines.append(f"{_shape_line(case)} tn={tn} ksplit={ks}   "
+                lines.append(f"{_shape_line(case)} tn={tn} ksplit={ks}{extra}   "
                              f"# {name}: {ms:.4f} ms (built-in choice {default_ms:.4f} ms)")
             else:   # within the timing noise of the built-in choice: keep it
                 lines.append(f"# {name}: built-in choice kept ({default_ms:.4f} ms; "
-                             f"best candidate tn={tn} ksplit={ks} {ms:.4f} ms)")
+                             f"best candidate tn={tn} ksplit={ks}{extra} {ms:.4f} ms)")
             del d
             torch.cuda.empty_cache()
     with open(out_path, "w") as f:

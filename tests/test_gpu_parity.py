@@ -345,6 +345,25 @@ def test_linear_graph_replay_with_new_inputs():
     assert torch.equal(out, eager)
 
 
+@pytest.mark.parametrize("name", ["decode", "tiny", "dense_mlp_t64"])
+def test_two_phase_launch_equals_two_launches(monkeypatch, name):
+    """Both projections in one persistent launch (single-CTA tiles) give the
+    same bits as one launch per projection: the items and their arithmetic
+    are the same, only the order in which CTAs take them differs."""
+    d = make_moe_case(CONFIGS[name], seed=3, device=DEV)
+    outs, names = {}, {}
+    for ph in ("1", "2"):
+        monkeypatch.setenv("MOELORA_TWO_PHASE", "0" if ph == "1" else "1")
+        outs[ph] = _gpu_forward(d).clone()
+        names[ph] = binding.moelora_last_launches()
+    assert "gemm_gate_up_down" in names["2"] and "gemm_gate_up_down" not in names["1"], names
+    assert torch.equal(outs["1"], outs["2"])
+    n = np_inputs(d, lazy=True)
+    tokens = np.arange(min(d["x"].shape[0], 16))
+    ok, msg = compare(outs["2"][torch.as_tensor(tokens, device=DEV)], _oracle_forward(n, tokens), name)
+    assert ok, msg
+
+
 def test_back_to_back_calls_on_one_stream():
     # Calls of different shapes (small-batch path with the fused row gather,
     # the multi-kernel align path, the dense linear) queued on one stream

@@ -68,7 +68,8 @@ def test_folder_loads_every_cfg_in_name_order(tmp_path):
 
 
 @pytest.mark.parametrize("text", ["moe tn=48\n", "moe ksplit=9\n", "attention T=4\n", "moe T=9-3\n", "moe bogus=1\n",
-                                  "moe T\n", "moe T=x\n", "moe T=5x\n", "moe T=-3\n", "moe T=4-\n", "moe k=4q\n"])
+                                  "moe T\n", "moe T=x\n", "moe T=5x\n", "moe T=-3\n", "moe T=4-\n", "moe k=4q\n",
+                                  "moe phases=3\n", "moe phases=0\n"])
 def test_malformed_tables_are_rejected_and_keep_the_old_one(tmp_path, text):
     binding.moelora_load_tuning(_write(tmp_path, "ok.cfg", "moe ksplit=1\n"))
     with pytest.raises(MoeLoraError):
