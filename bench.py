@@ -138,13 +138,18 @@ def workload_name(c):
 
 
 def source_hash():
-    """Hash of the GEMM kernel's sources: a DRAM-traffic figure captured by
-    ncu is reported only while the kernel it measured is unchanged."""
+    """Hash of the GEMM kernel's sources without their comments and blank
+    space: a DRAM-traffic figure captured by ncu is reported only while the
+    code it measured is unchanged (a comment edit keeps it)."""
+    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "lora_mixture_experts_gb300", "csrc")
     for n in ("gemm_tc.cu", "gemm_tc.cuh", "common.cuh"):
-        with open(os.path.join(d, n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(d, n)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

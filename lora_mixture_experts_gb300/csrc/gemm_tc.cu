@@ -1,8 +1,10 @@
 // Persistent tcgen05 grouped GEMM for the MoE-LoRA expert layer (sm_103a).
 //
-// One launch runs one projection phase of the layer (multi-LoRA MoE blog,
-// "Implementing multi-LoRA for MoE in vLLM": y = xW + xAB per projection,
-// the shrink z = xA and the expand zB, one GEMM per expert over its tokens):
+// One launch runs one projection phase of the layer, or on single-CTA tiles
+// both (gate_up items, then down items; see gemm_body).  Per projection
+// (multi-LoRA MoE blog, "Implementing multi-LoRA for MoE in vLLM": y = xW +
+// xAB, the shrink z = xA and the expand zB, one GEMM per expert over its
+// tokens):
 //
 //  * shrink items  -- z = X A[a,e]^T for the adapters present in a token tile,
 //    stacked r rows per adapter in one 128-row MMA tile.  The epilogue keeps,
