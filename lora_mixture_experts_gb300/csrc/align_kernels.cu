@@ -60,7 +60,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E,
       my_l = bv;
     }
   }
-  // softmax over the chosen logits (round 0 holds the largest)
+  // softmax over the chosen logits (the first pick holds the largest)
   const float m = __shfl_sync(0xffffffffu, my_l, 0);
   const float ex = (lane < k && my_id >= 0) ? expf(my_l - m) : 0.0f;
   float sum = ex;
