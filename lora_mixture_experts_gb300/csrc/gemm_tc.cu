@@ -169,15 +169,14 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-// One launch runs one phase (n_phases = 1: maps0 / p0), or on single-CTA
-// tiles both phases of the layer (n_phases = 2: gate_up items, then down
-// items, one item order and one claim counter).  A down item then waits for
-// its token tile's activation rows: every gate_up main item of the tile
-// counts on act_done[tile] once its rows are stored.  Items are claimed in
-// order and every CTA is resident, so the wait ends.
-// The body of both kernels below.  NPH is a template argument so that the
-// one-phase kernel reads its parameters at fixed offsets (no per-item
-// selection between p0 and p1: maps1 / p1 alias maps0 / p0 there).
+// The body of both kernels below.  A launch runs one phase (NPH = 1: maps0 /
+// p0, which maps1 / p1 alias), or on single-CTA tiles both phases of the
+// layer (NPH = 2: gate_up items, then down items, in one item order with one
+// claim counter).  A down item of a two-phase launch waits for its token
+// tile's activation rows: every gate_up main item of the tile counts on the
+// tile's counter once its rows are stored.  Items are claimed in order and
+// every CTA is resident, so the wait ends.  NPH is a template argument so
+// that the one-phase kernel reads its parameters at fixed offsets.
 template <int TN, bool PAIR, int NPH>
 __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps& maps1,
                                           const GemmParams& p0, const GemmParams& p1) {
