@@ -115,3 +115,24 @@ def test_timing_hook_host_only(lib):
     assert lib.moelora_set_timing_events(None, 0) == OK
     assert lib.moelora_set_timing_events(None, 3) == INVALID
     assert lib.moelora_set_timing_events(None, -1) == INVALID
+
+
+def test_shrink_splits_plan(lib, monkeypatch):
+    """The shrink items' K splits are planned on the host: their fp32 parts
+    take workspace only when the items are split.  Single-CTA tiles with a
+    long reduction are split by default; CTA-pair (256-token) tiles are not."""
+    decode = _d()                                      # 16-token tiles, K = 2880
+    prefill = _d(T=4096)                               # 256-token tiles on CTA pairs
+    base = {n: binding.moelora_workspace_bytes(d) for n, d in (("decode", decode), ("prefill", prefill))}
+    monkeypatch.setenv("MOELORA_SHRINK_SPLITS", "1")
+    one = {n: binding.moelora_workspace_bytes(d) for n, d in (("decode", decode), ("prefill", prefill))}
+    monkeypatch.setenv("MOELORA_SHRINK_SPLITS", "4")
+    four = {n: binding.moelora_workspace_bytes(d) for n, d in (("decode", decode), ("prefill", prefill))}
+    monkeypatch.delenv("MOELORA_SHRINK_SPLITS")
+    assert base["decode"] > one["decode"]              # split by default
+    assert base["prefill"] == one["prefill"]           # pairs keep one part
+    assert four["decode"] > base["decode"] and four["prefill"] > one["prefill"]
+    # the one- or two-phase choice needs no workspace of its own
+    monkeypatch.setenv("MOELORA_TWO_PHASE", "0")
+    assert binding.moelora_workspace_bytes(decode) == base["decode"]
+    assert binding.moelora_workspace_bytes(_d(L=0, r=0)) < base["decode"]
