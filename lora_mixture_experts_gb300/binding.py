@@ -113,6 +113,60 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _need(t, name: str, dtype, shape=None, optional: bool = False):
+    """Argument checks the C ABI cannot make (it sees only pointers and the
+    sizes passed in moelora_dims): dtype and shape of every tensor, before
+    anything is allocated or launched."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _same_device(*ts):
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) > 1:
+        raise ValueError(f"tensors on several devices: {sorted(str(d) for d in devs)}")
+
+
+def _check_layer(x, topk_weights, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, B_d, out, ws,
+                 topk_ids=None, router_logits=None, k=None):
+    if x.dim() != 2 or W_gate_up.dim() != 3:
+        raise ValueError("x must be [T, H] and W_gate_up [E, 2I, H]")
+    T, H = x.shape
+    E, two_i, _ = W_gate_up.shape
+    I = two_i // 2
+    bf = torch.bfloat16
+    _need(x, "x", bf)
+    _need(W_gate_up, "W_gate_up", bf, (E, 2 * I, H))
+    _need(W_down, "W_down", bf, (E, H, I))
+    if topk_ids is not None:
+        if topk_ids.dim() != 2:
+            raise ValueError("topk_ids must be [T, k]")
+        k = topk_ids.shape[1]
+        _need(topk_ids, "topk_ids", torch.int32, (T, k))
+        _need(topk_weights, "topk_weights", torch.float32, (T, k))
+    if router_logits is not None:
+        _need(router_logits, "router_logits", torch.float32, (T, E))
+    _need(lora_ids, "lora_ids", torch.int32, (T,))
+    if A_gu is not None:
+        if A_gu.dim() != 4:
+            raise ValueError("A_gu must be [L, E, r, H]")
+        L, r = A_gu.shape[0], A_gu.shape[2]
+        _need(A_gu, "A_gu", bf, (L, E, r, H))
+        _need(B_gu, "B_gu", bf, (L, E, 2 * I, r))
+        _need(A_d, "A_d", bf, (L, E, r, I))
+        _need(B_d, "B_d", bf, (L, E, H, r))
+    _need(out, "out", bf, (T, H), optional=True)
+    _need(ws, "ws", torch.uint8, optional=True)
+    _same_device(x, topk_ids, topk_weights, router_logits, lora_ids, W_gate_up, W_down, A_gu, B_gu,
+                 A_d, B_d, out, ws)
+
+
 def _check(st: int, where: str):
     if st != MOELORA_OK:
         raise MoeLoraError(st, where)
@@ -150,6 +204,10 @@ def moe_lora_align(topk_ids, lora_ids, E: int, L: int, block_m: int, ws=None, st
     """Returns (sorted_ids, blk_expert, seg_off, num_post_pad) device tensors."""
     lib = load()
     T, k = topk_ids.shape
+    _need(topk_ids, "topk_ids", torch.int32)
+    _need(lora_ids, "lora_ids", torch.int32, (T,))
+    _need(ws, "ws", torch.uint8, optional=True)
+    _same_device(topk_ids, lora_ids, ws)
     d = moelora_dims(T, k, E, 8, 8, L, 0)
     cap = lib.moelora_align_capacity(ctypes.byref(d), block_m)
     dev = topk_ids.device
@@ -173,6 +231,9 @@ def moe_lora_align_noalloc(topk_ids, lora_ids, E: int, L: int, block_m: int, str
     tensors are allocated here by torch only for the caller's convenience."""
     lib = load()
     T, k = topk_ids.shape
+    _need(topk_ids, "topk_ids", torch.int32)
+    _need(lora_ids, "lora_ids", torch.int32, (T,))
+    _same_device(topk_ids, lora_ids)
     d = moelora_dims(T, k, E, 8, 8, L, 0)
     cap = lib.moelora_align_capacity(ctypes.byref(d), block_m)
     dev = topk_ids.device
@@ -190,6 +251,8 @@ def moe_lora_forward(x, topk_ids, topk_weights, lora_ids, W_gate_up, W_down,
                      A_gu=None, B_gu=None, A_d=None, B_d=None, out=None, ws=None, stream=None):
     """The fused MoE-LoRA expert layer; returns out[T,H] bf16."""
     lib = load()
+    _check_layer(x, topk_weights, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, B_d, out, ws,
+                 topk_ids=topk_ids)
     d = dims_of(x, topk_ids, W_gate_up, W_down, A_gu)
     if out is None:
         out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
@@ -207,6 +270,10 @@ def moe_lora_route(logits, k: int, ids=None, weights=None, stream=None):
     """Router top-k on device: returns (topk_ids [T,k] int32, topk_weights [T,k] fp32)."""
     lib = load()
     T, E = logits.shape
+    _need(logits, "logits", torch.float32)
+    _need(ids, "ids", torch.int32, (T, k), optional=True)
+    _need(weights, "weights", torch.float32, (T, k), optional=True)
+    _same_device(logits, ids, weights)
     d = moelora_dims(T, k, E, 8, 8, 0, 0)
     if ids is None:
         ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
@@ -222,6 +289,8 @@ def moe_lora_forward_routed(x, router_logits, k: int, lora_ids, W_gate_up, W_dow
                             stream=None):
     """The layer with the router fused in (router logits [T,E] fp32, top-k)."""
     lib = load()
+    _check_layer(x, None, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, B_d, out, ws,
+                 router_logits=router_logits)
     T, H = x.shape
     E, two_i, _ = W_gate_up.shape
     L, r = (A_gu.shape[0], A_gu.shape[2]) if A_gu is not None else (0, 0)
@@ -244,6 +313,16 @@ def moe_lora_linear(x, lora_ids, W, A=None, B=None, out=None, ws=None, stream=No
     T, K = x.shape
     N = W.shape[0]
     L, r = (A.shape[0], A.shape[1]) if A is not None else (0, 0)
+    bf = torch.bfloat16
+    _need(x, "x", bf)
+    _need(lora_ids, "lora_ids", torch.int32, (T,))
+    _need(W, "W", bf, (N, K))
+    if A is not None:
+        _need(A, "A", bf, (L, r, K))
+        _need(B, "B", bf, (L, N, r))
+    _need(out, "out", bf, (T, N), optional=True)
+    _need(ws, "ws", torch.uint8, optional=True)
+    _same_device(x, lora_ids, W, A, B, out, ws)
     d = moelora_linear_dims(T, K, N, L, r)
     if out is None:
         out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
@@ -261,6 +340,17 @@ def moe_lora_merge_adapter(adapter: int, W_gate_up, W_down, A_gu, B_gu, A_d, B_d
     lib = load()
     E, two_i, H = W_gate_up.shape
     L, _, r, _ = A_gu.shape
+    I = two_i // 2
+    bf = torch.bfloat16
+    _need(W_gate_up, "W_gate_up", bf, (E, 2 * I, H))
+    _need(W_down, "W_down", bf, (E, H, I))
+    _need(A_gu, "A_gu", bf, (L, E, r, H))
+    _need(B_gu, "B_gu", bf, (L, E, 2 * I, r))
+    _need(A_d, "A_d", bf, (L, E, r, I))
+    _need(B_d, "B_d", bf, (L, E, H, r))
+    _need(W_gate_up_out, "W_gate_up_out", bf, (E, 2 * I, H), optional=True)
+    _need(W_down_out, "W_down_out", bf, (E, H, I), optional=True)
+    _same_device(W_gate_up, W_down, A_gu, B_gu, A_d, B_d, W_gate_up_out, W_down_out)
     d = moelora_dims(0, 1, E, H, two_i // 2, L, r)
     if W_gate_up_out is None:
         W_gate_up_out = torch.empty_like(W_gate_up)
