@@ -33,7 +33,11 @@
  *  - The workspace needs no initialisation: every byte a call reads was
  *    written earlier in the same call.
  *  - Not thread-safe per workspace: two calls that share a workspace must be
- *    ordered on one stream.
+ *    ordered on one stream.  Calls with separate workspaces may come from
+ *    several host threads; the process-wide state is the tuning table and the
+ *    timing hook (both guarded by a lock) and a per-device cache of launch
+ *    limits, filled on a device's first call (make one call per device before
+ *    calling from several threads on different devices).
  */
 #ifndef MOELORA_H_
 #define MOELORA_H_
