@@ -408,3 +408,28 @@ def test_pins_catch_source_mutation(monkeypatch, name):
     assert src.count(old) == 1, f"mutation site not unique: {old!r}"
     res = _run_pins(monkeypatch, _oracle_from_source(src.replace(old, new)))
     assert not all(v is True for v in res.values()), res
+
+
+# ------------------------------------------------ property test (hypothesis)
+def test_oracle_matches_brute_force_on_random_tiny_layers():
+    """The oracle against the scalar brute force on layers drawn by
+    hypothesis: sizes, routing (duplicates allowed), adapters including -1,
+    LoRA on or off."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=40, deadline=None, derandomize=True)
+    @hyp.given(st.integers(0, 5), st.integers(1, 6), st.integers(1, 5), st.integers(1, 4),
+               st.integers(1, 3), st.integers(0, 3), st.integers(1, 3), st.integers(0, 2 ** 31 - 1))
+    def check(T, H, I, E, k, L, r, seed):
+        rng = np.random.default_rng(seed)
+        d = _rand_layer(rng, T, H, I, E, min(k, E), L, r)
+        if T:
+            d["topk_ids"] = rng.integers(0, E, size=(T, min(k, E)))   # duplicates allowed
+        got = _fwd(d)
+        exp = _brute(d)
+        assert got.shape == (T, H)
+        if T:
+            assert _rel(got, exp) < 1e-12
+
+    check()
