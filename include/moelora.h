@@ -26,18 +26,23 @@
  *    kernels (bad ids, a bounded wait that ran out) are recorded in the
  *    workspace and read back with moelora_get_error.  Every wait in the
  *    kernels gives up after 2 s; the kernel then winds down and the next
- *    call runs normally.  Setting the environment variable
- *    MOELORA_FAULT_INJECT=shrink_wait makes the first GEMM phase of each
- *    call wait for shrink results that never come, so that a test can see
- *    MOELORA_ERR_TIMEOUT (the output of such a call is undefined).
+ *    call runs normally.  A call whose wait ran out has still returned
+ *    MOELORA_OK when it was enqueued; its output is undefined, and only
+ *    moelora_get_error shows the MOELORA_ERR_TIMEOUT.  Setting the
+ *    environment variable MOELORA_FAULT_INJECT=shrink_wait makes the first
+ *    GEMM phase of each call wait for shrink results that never come, so that
+ *    a test can see MOELORA_ERR_TIMEOUT.
  *  - The workspace needs no initialisation: every byte a call reads was
  *    written earlier in the same call.
  *  - Not thread-safe per workspace: two calls that share a workspace must be
  *    ordered on one stream.  Calls with separate workspaces may come from
  *    several host threads; the process-wide state is the tuning table and the
- *    timing hook (both guarded by a lock) and a per-device cache of launch
+ *    timing hook (both guarded by a lock), a per-device cache of launch
  *    limits, filled on a device's first call (make one call per device before
- *    calling from several threads on different devices).
+ *    calling from several threads on different devices), and
+ *    moe_lora_align_noalloc's scratch array with its device address, cached
+ *    per device under a lock together with the id of the context it was
+ *    found in (looked up again when that context has been replaced).
  */
 #ifndef MOELORA_H_
 #define MOELORA_H_
@@ -138,8 +143,10 @@ int moe_lora_align(const moelora_dims* d, const int32_t* topk_ids_dev,
  *     + 8*T*k + 4*E*(L+1) bytes) return MOELORA_ERR_WORKSPACE.
  *   - All calls share the one array: calls whose GPU work overlaps (on
  *     different streams without ordering) race; order them on one stream.
- *   - The first call on each device looks up the array's device address;
- *     make it before any stream capture.
+ *   - The first call on each device looks up the array's device address
+ *     (and looks it up again once the device's context has been destroyed
+ *     and created anew, as cudaDeviceReset does); make that call before any
+ *     stream capture.
  *   - Out-of-range ids are left out of the order as in moe_lora_align, but
  *     the device error flag is not readable (there is no workspace to pass to
  *     moelora_get_error).

@@ -127,14 +127,29 @@ def _need(t, name: str, dtype, shape=None, optional: bool = False):
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def _same_device(*ts):
+def _same_device(*ts, stream=None):
+    """The tensors share one device, which is the current CUDA device, and an
+    explicit stream belongs to it.  The library launches on the current
+    device with the pointers it is given, so tensors of another device would
+    fault on the GPU instead of raising here."""
     devs = {t.device for t in ts if t is not None}
     if len(devs) > 1:
         raise ValueError(f"tensors on several devices: {sorted(str(d) for d in devs)}")
+    if not devs:
+        return
+    dev = next(iter(devs))
+    if dev.type != "cuda":
+        return                      # _ptr reports host tensors
+    cur = torch.cuda.current_device()
+    if dev.index != cur:
+        raise ValueError(f"tensors on {dev} but the current CUDA device is cuda:{cur} "
+                         f"(call under torch.cuda.device({dev.index}))")
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"stream on {stream.device}, tensors on {dev}")
 
 
 def _check_layer(x, topk_weights, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, B_d, out, ws,
-                 topk_ids=None, router_logits=None, k=None):
+                 topk_ids=None, router_logits=None, k=None, stream=None):
     if x.dim() != 2 or W_gate_up.dim() != 3:
         raise ValueError("x must be [T, H] and W_gate_up [E, 2I, H]")
     T, H = x.shape
@@ -164,7 +179,7 @@ def _check_layer(x, topk_weights, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, 
     _need(out, "out", bf, (T, H), optional=True)
     _need(ws, "ws", torch.uint8, optional=True)
     _same_device(x, topk_ids, topk_weights, router_logits, lora_ids, W_gate_up, W_down, A_gu, B_gu,
-                 A_d, B_d, out, ws)
+                 A_d, B_d, out, ws, stream=stream)
 
 
 def _check(st: int, where: str):
@@ -207,7 +222,7 @@ def moe_lora_align(topk_ids, lora_ids, E: int, L: int, block_m: int, ws=None, st
     _need(topk_ids, "topk_ids", torch.int32)
     _need(lora_ids, "lora_ids", torch.int32, (T,))
     _need(ws, "ws", torch.uint8, optional=True)
-    _same_device(topk_ids, lora_ids, ws)
+    _same_device(topk_ids, lora_ids, ws, stream=stream)
     d = moelora_dims(T, k, E, 8, 8, L, 0)
     cap = lib.moelora_align_capacity(ctypes.byref(d), block_m)
     dev = topk_ids.device
@@ -233,7 +248,7 @@ def moe_lora_align_noalloc(topk_ids, lora_ids, E: int, L: int, block_m: int, str
     T, k = topk_ids.shape
     _need(topk_ids, "topk_ids", torch.int32)
     _need(lora_ids, "lora_ids", torch.int32, (T,))
-    _same_device(topk_ids, lora_ids)
+    _same_device(topk_ids, lora_ids, stream=stream)
     d = moelora_dims(T, k, E, 8, 8, L, 0)
     cap = lib.moelora_align_capacity(ctypes.byref(d), block_m)
     dev = topk_ids.device
@@ -252,7 +267,7 @@ def moe_lora_forward(x, topk_ids, topk_weights, lora_ids, W_gate_up, W_down,
     """The fused MoE-LoRA expert layer; returns out[T,H] bf16."""
     lib = load()
     _check_layer(x, topk_weights, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, B_d, out, ws,
-                 topk_ids=topk_ids)
+                 topk_ids=topk_ids, stream=stream)
     d = dims_of(x, topk_ids, W_gate_up, W_down, A_gu)
     if out is None:
         out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
@@ -273,7 +288,7 @@ def moe_lora_route(logits, k: int, ids=None, weights=None, stream=None):
     _need(logits, "logits", torch.float32)
     _need(ids, "ids", torch.int32, (T, k), optional=True)
     _need(weights, "weights", torch.float32, (T, k), optional=True)
-    _same_device(logits, ids, weights)
+    _same_device(logits, ids, weights, stream=stream)
     d = moelora_dims(T, k, E, 8, 8, 0, 0)
     if ids is None:
         ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
@@ -290,7 +305,7 @@ def moe_lora_forward_routed(x, router_logits, k: int, lora_ids, W_gate_up, W_dow
     """The layer with the router fused in (router logits [T,E] fp32, top-k)."""
     lib = load()
     _check_layer(x, None, lora_ids, W_gate_up, W_down, A_gu, B_gu, A_d, B_d, out, ws,
-                 router_logits=router_logits)
+                 router_logits=router_logits, stream=stream)
     T, H = x.shape
     E, two_i, _ = W_gate_up.shape
     L, r = (A_gu.shape[0], A_gu.shape[2]) if A_gu is not None else (0, 0)
@@ -322,7 +337,7 @@ def moe_lora_linear(x, lora_ids, W, A=None, B=None, out=None, ws=None, stream=No
         _need(B, "B", bf, (L, N, r))
     _need(out, "out", bf, (T, N), optional=True)
     _need(ws, "ws", torch.uint8, optional=True)
-    _same_device(x, lora_ids, W, A, B, out, ws)
+    _same_device(x, lora_ids, W, A, B, out, ws, stream=stream)
     d = moelora_linear_dims(T, K, N, L, r)
     if out is None:
         out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
@@ -350,7 +365,7 @@ def moe_lora_merge_adapter(adapter: int, W_gate_up, W_down, A_gu, B_gu, A_d, B_d
     _need(B_d, "B_d", bf, (L, E, H, r))
     _need(W_gate_up_out, "W_gate_up_out", bf, (E, 2 * I, H), optional=True)
     _need(W_down_out, "W_down_out", bf, (E, H, I), optional=True)
-    _same_device(W_gate_up, W_down, A_gu, B_gu, A_d, B_d, W_gate_up_out, W_down_out)
+    _same_device(W_gate_up, W_down, A_gu, B_gu, A_d, B_d, W_gate_up_out, W_down_out, stream=stream)
     d = moelora_dims(0, 1, E, H, two_i // 2, L, r)
     if W_gate_up_out is None:
         W_gate_up_out = torch.empty_like(W_gate_up)
@@ -374,6 +389,7 @@ def moelora_tuning_entries() -> int:
 
 
 def moelora_get_error(ws, stream=None) -> int:
+    _same_device(ws, stream=stream)
     return load().moelora_get_error(_ptr(ws), _stream(stream))
 
 

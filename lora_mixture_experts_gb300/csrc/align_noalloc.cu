@@ -18,8 +18,12 @@
 //  * all calls share the one array, so two calls whose work overlaps on the
 //    GPU (different streams, no ordering between them) race and may both
 //    produce wrong results; order them on one stream;
-//  * the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress); make that first call outside any stream capture.
+//  * the first call on each device (and again after the device's context
+//    was destroyed and created anew) looks up the array's device address
+//    with cudaGetSymbolAddress; make that first call outside any stream
+//    capture.
+#include <cuda.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -36,21 +40,71 @@ constexpr int kMaxDevices = 64;
 // passed to kernels.
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
+// Cached device address of the array, per device, with the id of the
+// context it was looked up in.  A context torn down and made again (for
+// instance after cudaDeviceReset) reloads the library's module and moves the
+// array, so a cached address is used only while the current context's id is
+// the one it was found in.
+struct CachedAddr {
+  unsigned long long ctx_id;
+  void* ptr;
+};
 std::mutex g_addr_mu;
-void* g_addr[kMaxDevices] = {};
+CachedAddr g_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current).  nullptr on failure.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, looked up once through the
+// runtime (the library links only the runtime).
+bool context_id_fns(CtxGetCurrentFn& get_current, CtxGetIdFn& get_id) {
+  static CtxGetCurrentFn cur = nullptr;
+  static CtxGetIdFn idf = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      idf = reinterpret_cast<CtxGetIdFn>(p);
+  }
+  get_current = cur;
+  get_id = idf;
+  return cur && idf;
+}
+
+// Id of the current context, 0 if there is none yet or it cannot be read.
+unsigned long long current_context_id(CtxGetCurrentFn get_current, CtxGetIdFn get_id) {
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// cudaGetSymbolAddress (with that device current) on the first call in each
+// context.  nullptr on failure.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CtxGetCurrentFn get_current;
+  CtxGetIdFn get_id;
   std::lock_guard<std::mutex> lk(g_addr_mu);
-  if (!g_addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_addr[dev] = ptr;
-  }
-  return g_addr[dev];
+  if (!context_id_fns(get_current, get_id)) return nullptr;
+  const unsigned long long id = current_context_id(get_current, get_id);
+  if (id != 0 && g_addr[dev].ptr && g_addr[dev].ctx_id == id) return g_addr[dev].ptr;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+  // (the lookup makes the device's primary context current if it was not)
+  const unsigned long long id_now = current_context_id(get_current, get_id);
+  g_addr[dev] = {id_now, ptr};
+  return ptr;
 }
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }

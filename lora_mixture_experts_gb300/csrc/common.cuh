@@ -285,8 +285,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// SiLU(v) = v * sigmoid(v) = v / (1 + e^-v), as v times the correctly rounded
-// reciprocal (for very negative v the reciprocal of +inf is 0, giving -0).
+// SiLU(v) = v * sigmoid(v) = v / (1 + e^-v), with the fast exponential and
+// the fast (approximate) divide; for very negative v, e^-v is +inf and the
+// quotient is -0.
 __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // 32 lanes x 32 bit, 32 consecutive columns per thread.

@@ -56,3 +56,43 @@ def test_linear_route_and_align_checks(lib):
         binding.moe_lora_route(torch.zeros(4, 8, dtype=torch.float16), 2)
     with pytest.raises(ValueError, match="topk_ids: dtype"):
         binding.moe_lora_align(torch.zeros(4, 2, dtype=torch.int64), lo, 8, 1, 16)
+
+
+class _OnDevice:
+    """Stands in for a tensor on a CUDA device (there is none on this host):
+    only the attributes the binding's checks read."""
+
+    def __init__(self, index, shape, dtype):
+        self.device = torch.device("cuda", index)
+        self.shape = torch.Size(shape)
+        self.dtype = dtype
+
+    def dim(self):
+        return len(self.shape)
+
+
+class _Stream:
+    def __init__(self, index):
+        self.device = torch.device("cuda", index)
+
+
+def test_tensors_off_the_current_device_are_rejected(lib, monkeypatch):
+    # the library launches on the current device with the pointers it gets:
+    # tensors of another device must raise before anything is launched
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    ids = _OnDevice(0, (4, 2), torch.int32)
+    lo = _OnDevice(0, (4,), torch.int32)
+    with pytest.raises(ValueError, match="current CUDA device is cuda:1"):
+        binding.moe_lora_align(ids, lo, 8, 1, 16)
+    with pytest.raises(ValueError, match="current CUDA device is cuda:1"):
+        binding.moe_lora_align_noalloc(ids, lo, 8, 1, 16)
+    with pytest.raises(ValueError, match="current CUDA device is cuda:1"):
+        binding.moelora_get_error(_OnDevice(0, (64,), torch.uint8))
+
+
+def test_stream_of_another_device_is_rejected(lib, monkeypatch):
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    ids = _OnDevice(0, (4, 2), torch.int32)
+    lo = _OnDevice(0, (4,), torch.int32)
+    with pytest.raises(ValueError, match="stream on cuda:1"):
+        binding.moe_lora_align(ids, lo, 8, 1, 16, stream=_Stream(1))

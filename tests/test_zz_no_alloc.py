@@ -3,10 +3,11 @@
 moe_lora_align_noalloc keeps its scratch in a fixed array inside the
 library instead of a caller workspace, for code that runs during CUDA-graph
 capture, plug-ins without an allocator, or servers whose device memory is
-all reserved by their own pool.  Its results must be identical to
-moe_lora_align's (the align is integer work: bit-exact), on two calls in a
-row (the shared array keeps the previous call's contents), and it must
-reject sizes beyond its fixed scratch.
+all reserved by their own pool.  Its results must equal the oracle's align
+definition bit for bit (the align is integer work), and moe_lora_align's, on
+two calls in a row (the shared array keeps the previous call's contents);
+it must handle an empty batch, leave out entries with out-of-range ids as
+moe_lora_align does, and reject sizes beyond its fixed scratch.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
@@ -19,6 +20,7 @@ import torch
 
 from lora_mixture_experts_gb300 import binding
 from lora_mixture_experts_gb300.inputs import CONFIGS, make_routing
+from oracle import moe_lora_ref as ref
 
 pytestmark = pytest.mark.gpu
 
@@ -27,24 +29,66 @@ def _same(a, b):
     return all(torch.equal(x, y) for x, y in zip(a, b))
 
 
+def _matches_oracle(res, ids, lo, E, L, bm):
+    s, b, seg, npp = res
+    exp = ref.align_ref(ids.cpu().numpy(), lo.cpu().numpy(), E, L, bm)
+    P = exp["num_post_pad"]
+    assert int(npp.item()) == P
+    assert np.array_equal(s[:P].cpu().numpy(), exp["sorted_ids"])
+    assert np.array_equal(b[:P // bm].cpu().numpy(), exp["blk_expert"])
+    assert np.array_equal(seg.cpu().numpy(), exp["seg_off"])
+    assert bool((s[P:] == ids.numel()).all())
+
+
 @pytest.mark.parametrize("name", ["decode", "prefill", "skewed"])
-def test_noalloc_align_matches_workspace_align_twice(name):
+def test_noalloc_align_matches_oracle_and_workspace_align_twice(name):
     c = CONFIGS[name]
     ids, _, lo = make_routing(c, seed=0)
     ids, lo = ids.cuda(), lo.cuda()
-    ref = binding.moe_lora_align(ids, lo, c.E, c.L, 16)
+    with_ws = binding.moe_lora_align(ids, lo, c.E, c.L, 16)
     first = binding.moe_lora_align_noalloc(ids, lo, c.E, c.L, 16)
     torch.cuda.synchronize()
-    assert _same(ref, first)
+    _matches_oracle(first, ids, lo, c.E, c.L, 16)
+    assert _same(with_ws, first)
     # a second call with other routing, then the first routing again: the
     # shared scratch keeps the previous call's contents and must not leak
     ids2, _, lo2 = make_routing(c, seed=1)
-    ref2 = binding.moe_lora_align(ids2.cuda(), lo2.cuda(), c.E, c.L, 16)
-    second = binding.moe_lora_align_noalloc(ids2.cuda(), lo2.cuda(), c.E, c.L, 16)
+    ids2, lo2 = ids2.cuda(), lo2.cuda()
+    second = binding.moe_lora_align_noalloc(ids2, lo2, c.E, c.L, 16)
     third = binding.moe_lora_align_noalloc(ids, lo, c.E, c.L, 16)
     torch.cuda.synchronize()
-    assert _same(ref2, second)
-    assert _same(ref, third)
+    _matches_oracle(second, ids2, lo2, c.E, c.L, 16)
+    _matches_oracle(third, ids, lo, c.E, c.L, 16)
+
+
+def test_noalloc_align_empty_batch():
+    # T = 0: no entries, no blocks, every segment offset 0
+    ids = torch.empty((0, 4), dtype=torch.int32, device="cuda")
+    lo = torch.empty((0,), dtype=torch.int32, device="cuda")
+    res = binding.moe_lora_align_noalloc(ids, lo, 8, 3, 16)
+    torch.cuda.synchronize()
+    assert int(res[3].item()) == 0
+    assert bool((res[2] == 0).all())
+    # and a normal call right after it
+    c = CONFIGS["tiny"]
+    ids, _, lo = make_routing(c, seed=0)
+    res = binding.moe_lora_align_noalloc(ids.cuda(), lo.cuda(), c.E, c.L, 16)
+    torch.cuda.synchronize()
+    _matches_oracle(res, ids, lo, c.E, c.L, 16)
+
+
+def test_noalloc_align_leaves_out_bad_ids():
+    # entries whose expert or adapter id is out of range are left out of the
+    # order, as moe_lora_align leaves them out
+    ids = torch.tensor([[0, 1], [1, 7], [2, 0]], dtype=torch.int32, device="cuda")
+    lo = torch.tensor([0, -1, 5], dtype=torch.int32, device="cuda")   # 7 >= E, 5 >= L
+    s, b, seg, npp = binding.moe_lora_align_noalloc(ids, lo, 4, 2, 4)
+    with_ws = binding.moe_lora_align(ids, lo, 4, 2, 4)
+    torch.cuda.synchronize()
+    assert _same((s, b, seg, npp), with_ws)
+    P = int(npp.item())
+    kept = sorted(int(v) for v in s[:P].cpu() if int(v) != ids.numel())
+    assert kept == [0, 1, 2]          # token 0's two entries and token 1's expert 1
 
 
 def test_noalloc_align_rejects_sizes_beyond_its_scratch():
