@@ -15,6 +15,16 @@ its own batch (no collective on the data path); the timed region is
 bracketed by a barrier and a synchronize, and the slowest rank's time
 counts.  Rank 0 prints one JSON line.
 
+With the decode batch as the headline (the default), one GPU, the other
+workloads (prefill, skewed, the dense linear and the dense MLP at T = 1, 8,
+64, 512) are timed after it, about a quarter second each, and reported under
+`per_config` with their own roofline, clocks and parity.  Every timed
+output is compared with the oracle over its whole batch (`parity`).
+
+A tensor-bound kernel is rated against the burst bf16 peak when its timed
+loop is shorter than 1.5 s (every default loop), else against the sustained
+(power-capped) one; `roofline.peak_source` names the peak used.
+
 --impl reference times the CPU oracle (float64 numpy) on this host's cores
 on a bounded sample of the same workload; only rank 0 works under torchrun.
 """
@@ -46,6 +56,12 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bounded CPU work of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the oracle comparison of the timed outputs")
+    ap.add_argument("--per-config", default=None,
+                    help="comma-separated workloads timed after the headline, each reported under "
+                         "per_config ('none' for none; default: every other workload when the "
+                         "headline is the decode batch)")
     ap.add_argument("--tuning", default=os.path.join(ROOT, "lora_mixture_experts_gb300", "tuning"),
                     help="tuned launch-choice table (file or folder); 'none' = built-in choices")
     return ap.parse_args()
@@ -284,23 +300,59 @@ def run_reference(args, rank, world):
     }
 
 
-def run_ours(args, rank, world, device):
-    import torch
-    import numpy as np
-    from lora_mixture_experts_gb300 import binding, roofline
-    from lora_mixture_experts_gb300.inputs import CONFIGS, LinearCase, make_linear_case, make_moe_case
+class _LazyBits:
+    """Indexable host view of a device bf16 tensor: an index copies only that
+    slice to the host (as bf16 bit patterns), so the oracle reads one
+    expert's weights at a time instead of a copy of the whole set."""
 
-    binding.load(build_if_missing=True)
-    tuning = None
-    if args.tuning and args.tuning != "none" and os.path.exists(args.tuning):
-        binding.moelora_load_tuning(args.tuning)
-        tuning = os.path.relpath(args.tuning, ROOT)
-    case = CONFIGS[args.config]
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        from lora_mixture_experts_gb300.inputs import bf16_bits
+        return bf16_bits(self.t[idx])
+
+
+def oracle_full(case, d):
+    """The oracle's output for every token of the batch in `d` (device
+    tensors), weights read one expert at a time."""
+    import torch
+    from oracle import moe_lora_ref as ref
+    from lora_mixture_experts_gb300.inputs import LinearCase, bf16_bits
+    if isinstance(case, LinearCase):
+        return ref.moe_lora_linear_ref(bf16_bits(d["x"]), d["lora_ids"].cpu().numpy(), bf16_bits(d["W"]),
+                                       bf16_bits(d["A"]), bf16_bits(d["B"]))
+    h = {}
+    for k, v in d.items():
+        if v.dtype == torch.bfloat16:
+            h[k] = bf16_bits(v) if k == "x" else _LazyBits(v)
+        else:
+            h[k] = v.cpu().numpy()
+    return ref.moe_lora_forward_ref(h["x"], h["topk_ids"], h["topk_weights"], h["lora_ids"],
+                                    h["W_gate_up"], h["W_down"], h.get("A_gu"), h.get("B_gu"),
+                                    h.get("A_d"), h.get("B_d"))
+
+
+# a kernel timed inside a loop shorter than this is rated against the burst
+# bf16 peak, a longer one against the sustained (power-capped) peak
+SUSTAINED_AFTER_S = 1.5
+
+
+def measure(case, args, steps, warmup, rank, world, device, peaks, sampler, e2e=True, target_s=0.25):
+    """Times one workload: `steps` calls of the whole layer after `warmup`
+    calls (steps=None: as many as take about target_s; device time between
+    CUDA events, max over ranks), then the same
+    steps with an event around every kernel of the call (the dominant
+    kernel's time), then the end-to-end loop through the public API.
+    Returns (result dict, output tensor, device inputs)."""
+    import torch
+    from lora_mixture_experts_gb300 import binding, roofline
+    from lora_mixture_experts_gb300.inputs import LinearCase, make_linear_case, make_moe_case
+
     linear = isinstance(case, LinearCase)
     seed = rank_seed(rank)
     d = make_linear_case(case, seed=seed, device=device) if linear else make_moe_case(case, seed=seed, device=device)
-    peaks = roofline.load_peaks(ROOT)
-
     if linear:
         dims = binding.moelora_linear_dims(case.T, case.K, case.N, case.L, case.r)
         ws = binding.alloc_workspace(binding.moelora_linear_workspace_bytes(dims), device)
@@ -308,8 +360,7 @@ def run_ours(args, rank, world, device):
 
         def fwd(x=d["x"], lo=d["lora_ids"]):
             binding.moe_lora_linear(x, lo, d["W"], d["A"], d["B"], out=out, ws=ws)
-        lo_np = d["lora_ids"].cpu().numpy()
-        layer = roofline.linear_work(lo_np, case.K, case.N, case.r)
+        layer = roofline.linear_work(d["lora_ids"].cpu().numpy(), case.K, case.N, case.r)
         kernel_work = {"gemm_linear": layer}
         step_inputs = ["x", "lora_ids"]
     else:
@@ -327,36 +378,39 @@ def run_ours(args, rank, world, device):
                        "gemm_gate_up_down": roofline.Work(gu.bytes + dn.bytes, gu.flops + dn.flops)}
         step_inputs = ["x", "topk_ids", "topk_weights", "lora_ids"]
 
-    stream = torch.cuda.current_stream()
     fwd()
     torch.cuda.synchronize()
     status = binding.moelora_get_error(ws)
     if status != 0:
-        raise RuntimeError(f"device status {binding.moelora_status_string(status)}")
+        raise RuntimeError(f"{case.name}: device status {binding.moelora_status_string(status)}")
     names = binding.moelora_last_launches()
     nl = len(names)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         fwd()
     torch.cuda.synchronize()
+    if steps is None:
+        # about `target_s` of timed calls, 20 to 2000 of them
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(3):
+            fwd()
+        c1.record()
+        torch.cuda.synchronize()
+        steps = int(min(2000, max(20, target_s * 1e3 / (c0.elapsed_time(c1) / 3))))
 
-    K = args.steps
+    K = steps
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    dev_index = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[device.index] \
-        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(device.index)
-    sampler = ClockSampler(dev_index)
-    sampler.wait_first()
-    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     e0.record()
-    for i in range(K):
+    for _ in range(K):
         fwd()
     e1.record()
     torch.cuda.synchronize()
-    t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1) / K
@@ -382,10 +436,8 @@ def run_ours(args, rank, world, device):
     t_wall2 = time.time()
     binding.moelora_set_timing_events(None)
     ms_profiled = p0.elapsed_time(p1) / K
-    sampler_summary = sampler.summary(t_wall0, t_wall2)
-    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall2)
 
-    # per-kernel device time over the timed steps
     per = {}
     for i in range(K):
         for j in range(nl):
@@ -393,65 +445,25 @@ def run_ours(args, rank, world, device):
     kernel_ms = {n: sum(v) / len(v) for n, v in per.items()}
     dom = max(kernel_work, key=lambda n: kernel_ms.get(n, 0.0))
     w = kernel_work[dom]
-    sustained = True
+    region_s = K * ms / 1e3
+    sustained = region_s >= SUSTAINED_AFTER_S
     bound = roofline.bound_of(w, peaks, sustained)
     dur_s = kernel_ms[dom] / 1e3
+    tc_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     if bound == "hbm":
         achieved, peak, unit = w.bytes / dur_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        peak_name = "HBM copy"
     else:
-        achieved, peak, unit = w.flops / dur_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
-    traffic = load_traffic(args.config, dom)
-
-    # end to end through the public API: the step's inputs packed in one
-    # pinned host buffer (each at a 256-byte offset) and copied in one
-    # transfer, the forward on device views of that buffer, the result read
-    # back, every step
-    offs, nbytes = {}, 0
-    for k in step_inputs:
-        offs[k] = nbytes
-        nbytes += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
-    host_buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    dev_buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
-
-    def view(buf, k):
-        n = d[k].numel() * d[k].element_size()
-        return buf[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
-    for k in step_inputs:
-        view(host_buf, k).copy_(d[k].cpu())
-    dev_in = {k: view(dev_buf, k) for k in step_inputs}
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = nbytes
-    d2h = out.numel() * out.element_size()
-
-    def e2e_step():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        fwd(*[dev_in[k] for k in step_inputs])
-        out_h.copy_(out, non_blocking=True)
-    for _ in range(min(args.warmup, 5)):
-        e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for _ in range(K):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / K
-    e2e_s = reduce_max(e2e_s, world, device)
-
-    T = case.T
-    value = T * world / (ms / 1e3)
+        achieved, peak, unit = w.flops / dur_s / 1e12, peaks[tc_key], "TFLOP/s"
+        peak_name = ("bf16 sustained" if sustained else "bf16 burst") + \
+            f" (timed region {region_s:.2f} s)"
+    traffic = load_traffic(case.name, dom)
     res = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(case), "tokens_per_step_per_gpu": T,
-                   "l2": "weights larger than the 129 MB L2, no flush between steps",
-                   "parallelism": f"replicas x{world} (independent batches, no collective)",
-                   "tuning": tuning or "built-in choices"},
+        "ms_per_step": ms, "steps": K, "warmup": warmup,
+        "value": case.T * world / (ms / 1e3), "unit": "tokens/s",
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peaks['source']} ({'bf16 sustained' if unit == 'TFLOP/s' else 'HBM copy'})",
+                     "peak_source": f"{peaks['source']} ({peak_name})",
                      "algorithmic_bytes": w.bytes, "algorithmic_flops": w.flops,
                      "kernel_ms": kernel_ms[dom]},
         "layer_roofline": {"bound": roofline.bound_of(layer, peaks, sustained),
@@ -460,24 +472,121 @@ def run_ours(args, rank, world, device):
                            "bytes": layer.bytes, "flops": layer.flops},
         "kernel_ms": kernel_ms,
         "ms_per_step_with_kernel_events": ms_profiled,
-        "e2e": {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
         "gpu_launches": nl * K,
-        "clocks": sampler_summary,
+        "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        hostw = host_inputs({k: v for k, v in d.items()})
-        tokens = sample_tokens(case, oracle_budget_tokens(case))
-        v, sample, y = oracle_baseline(case, hostw, args.cpu_seconds, tokens)
-        res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                               "sample": sample}
-        # the timed calls' output against the oracle's rows of the sampled tokens
-        res["parity"] = parity_summary(out[torch.as_tensor(tokens, device=out.device)], y)
+    if e2e:
+        # end to end through the public API: the step's inputs packed in one
+        # pinned host buffer (each at a 256-byte offset) and copied in one
+        # transfer, the forward on device views of that buffer, the result
+        # read back, every step
+        offs, nbytes = {}, 0
+        for k in step_inputs:
+            offs[k] = nbytes
+            nbytes += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
+        host_buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        dev_buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+        def view(buf, k):
+            n = d[k].numel() * d[k].element_size()
+            return buf[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
+        for k in step_inputs:
+            view(host_buf, k).copy_(d[k].cpu())
+        dev_in = {k: view(dev_buf, k) for k in step_inputs}
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            dev_buf.copy_(host_buf, non_blocking=True)
+            fwd(*[dev_in[k] for k in step_inputs])
+            out_h.copy_(out, non_blocking=True)
+        for _ in range(min(warmup, 5)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = reduce_max((time.perf_counter() - t0) / K, world, device)
+        res["e2e"] = {"value": case.T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+                      "d2h_bytes_per_step": out.numel() * out.element_size()}
+    # the last timed call's output is the forward of these inputs again
+    fwd()
+    torch.cuda.synchronize()
+    return res, out, d
+
+
+# the workloads timed after the headline in a default run (each one's own
+# line under `per_config`); the headline stays the decode batch
+PER_CONFIG = ("prefill", "skewed", "dense_t1", "dense_t8", "dense_t64", "dense_t512",
+              "dense_mlp_t1", "dense_mlp_t8", "dense_mlp_t64", "dense_mlp_t512")
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    from lora_mixture_experts_gb300 import binding, roofline
+    from lora_mixture_experts_gb300.inputs import CONFIGS
+
+    binding.load(build_if_missing=True)
+    tuning = None
+    if args.tuning and args.tuning != "none" and os.path.exists(args.tuning):
+        binding.moelora_load_tuning(args.tuning)
+        tuning = os.path.relpath(args.tuning, ROOT)
+    case = CONFIGS[args.config]
+    peaks = roofline.load_peaks(ROOT)
+    dev_index = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[device.index] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(device.index)
+    sampler = ClockSampler(dev_index)
+    sampler.wait_first()
+    try:
+        m, out, d = measure(case, args, args.steps, args.warmup, rank, world, device, peaks, sampler)
+        res = {
+            "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_name(case), "tokens_per_step_per_gpu": case.T,
+                       "l2": "weights larger than the 129 MB L2, no flush between steps",
+                       "parallelism": f"replicas x{world} (independent batches, no collective)",
+                       "tuning": tuning or "built-in choices"},
+        }
+        for k in ("roofline", "layer_roofline", "kernel_ms", "ms_per_step_with_kernel_events", "e2e",
+                  "gpu_launches", "clocks"):
+            res[k] = m[k]
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            hostw = host_inputs({k: v for k, v in d.items()})
+            tokens = sample_tokens(case, oracle_budget_tokens(case))
+            v, sample, _ = oracle_baseline(case, hostw, args.cpu_seconds, tokens)
+            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                   "sample": sample}
+        if rank == 0 and not args.no_parity:
+            # the timed output against the oracle over the whole batch
+            res["parity"] = parity_summary(out, oracle_full(case, d))
+        del d, out
+        per_names = [n for n in (args.per_config.split(",") if args.per_config else []) if n and n != "none"]
+        if world == 1 and per_names:
+            res["per_config"] = {}
+            for name in per_names:
+                c = CONFIGS[name]
+                torch.cuda.empty_cache()
+                # about a quarter second of timed calls
+                m, out, d = measure(c, args, None, max(args.warmup // 10, 5), rank, world, device, peaks,
+                                    sampler)
+                m["workload"] = workload_name(c)
+                if not args.no_parity:
+                    m["parity"] = parity_summary(out, oracle_full(c, d))
+                res["per_config"][name] = m
+                del d, out
+    finally:
+        sampler.stop()
     return res
 
 
 def main():
     args = parse_args()
+    if args.per_config is None:
+        args.per_config = ",".join(PER_CONFIG) if args.config == "decode" else "none"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

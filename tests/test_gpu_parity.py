@@ -3,10 +3,12 @@
 * align: bit-exact against the oracle's definition for every workload's
   routing and for edge cases (block_m 1..128, empty experts, all tokens on one
   expert, adapters absent);
-* forward: the tiny and decode workloads in full; prefill, skewed and the
-  dense linear at full size on sampled tokens the oracle computes one by
-  one; random small shapes with ragged tails (H not a multiple of 128, I not
-  a multiple of 64, T = 1, k = E, every LoRA rank, no LoRA);
+* forward: every workload at full size, every token of the batch compared
+  element by element with the oracle (tiny, decode, prefill, skewed, the
+  dense linear and the dense MLP at T = 1, 8, 64, 512, in the built-in and
+  the tuned launch configuration); random small shapes with ragged tails (H
+  not a multiple of 128, I not a multiple of 64, T = 1, k = E, every LoRA
+  rank, no LoRA);
 * determinism, CUDA-graph capture/replay, and the device-side bad-index flag.
 """
 import numpy as np
@@ -108,13 +110,31 @@ def test_align_bad_index_flag():
 
 
 # ------------------------------------------------------------------ forward
-def _run_parity(d, tokens=None, what=""):
+# oracle outputs of the full-size workloads, shared by the tests that run one
+# workload in several launch configurations
+_ORACLE = {}
+
+
+def _large(d):
+    return sum(v.numel() * v.element_size() for v in d.values()) > (256 << 20)
+
+
+def _run_parity(d, tokens=None, what="", key=None):
+    """The layer on the GPU against the oracle: every token of the batch
+    (or the given tokens), element by element.  Large weights are copied to
+    the host one expert at a time as the oracle reaches them."""
     out = _gpu_forward(d)
     torch.cuda.synchronize()
-    n = np_inputs(d, lazy=tokens is not None)
-    exp = _oracle_forward(n, tokens)
+    if key is not None and key in _ORACLE:
+        exp = _ORACLE[key]
+    else:
+        n = np_inputs(d, lazy=tokens is not None or _large(d))
+        exp = _oracle_forward(n, tokens)
+        if key is not None:
+            _ORACLE[key] = exp
     got = out if tokens is None else out[torch.as_tensor(tokens, device=out.device)]
     ok, msg = compare(got, exp, what)
+    print(msg)
     assert ok, msg
     return out
 
@@ -124,31 +144,46 @@ def test_forward_tiny():
     _run_parity(d, what="tiny")
 
 
-def test_forward_decode():
-    d = make_moe_case(CONFIGS["decode"], seed=0, device=DEV)
-    _run_parity(d, what="decode")
-
-
-def test_forward_prefill_sampled():
-    d = make_moe_case(CONFIGS["prefill"], seed=0, device=DEV)
-    rng = np.random.default_rng(0)
-    tokens = np.sort(rng.choice(4096, size=24, replace=False))
-    tokens[0], tokens[-1] = 0, 4095
-    _run_parity(d, tokens=tokens, what="prefill sample")
+@pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
+def test_forward_decode(tuned):
+    # the tuned table is the launch configuration bench.py times (32-token
+    # tiles, both projections in one launch)
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    binding.moelora_load_tuning(table if tuned else None)
+    try:
+        d = make_moe_case(CONFIGS["decode"], seed=0, device=DEV)
+        _run_parity(d, what=f"decode ({'tuned' if tuned else 'built-in'})", key="decode")
+    finally:
+        binding.moelora_load_tuning(None)
 
 
 @pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
-def test_forward_skewed_sampled(tuned):
+def test_forward_prefill_full(tuned):
+    # all 4096 tokens (16384 routed pairs on 2-SM tiles) against the oracle
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    binding.moelora_load_tuning(table if tuned else None)
+    try:
+        d = make_moe_case(CONFIGS["prefill"], seed=0, device=DEV)
+        _run_parity(d, what=f"prefill (all 4096 tokens, {'tuned' if tuned else 'built-in'})",
+                    key="prefill")
+    finally:
+        binding.moelora_load_tuning(None)
+
+
+@pytest.mark.parametrize("tuned", [False, True], ids=["built_in", "tuned_table"])
+def test_forward_skewed_full(tuned):
     # the tuned table (the launch configuration bench.py times) runs this
-    # workload on larger token tiles than the built-in choice
+    # workload on larger token tiles than the built-in choice; all 256 tokens
+    # (1536 routed pairs over the Zipf-loaded experts) against the oracle
     import os
     table = os.path.join(os.path.dirname(binding.__file__), "tuning")
     binding.moelora_load_tuning(table if tuned else None)
     try:
         d = make_moe_case(CONFIGS["skewed"], seed=0, device=DEV)
-        rng = np.random.default_rng(1)
-        tokens = np.sort(rng.choice(256, size=12, replace=False))
-        _run_parity(d, tokens=tokens, what="skewed sample")
+        _run_parity(d, what=f"skewed (all 256 tokens, {'tuned' if tuned else 'built-in'})",
+                    key="skewed")
     finally:
         binding.moelora_load_tuning(None)
 
@@ -234,6 +269,13 @@ def test_forward_random_shapes(shape):
 
 
 def test_forward_many_experts_top8():
+    # A stress shape beyond the five workloads: gate-weighted sums of eight
+    # Zipf-routed pairs put some outputs at 9-10 x RMS, where one bf16 ulp
+    # of the output is 2-4 x the max-abs bound's 3e-2 x RMS; with the
+    # activation rounded to bf16 as the down GEMM's operand, a float64
+    # emulation of the kernel's rounding points already exceeds the bound at
+    # 1-3 of the 131k elements on 2 of 3 seeds.  Compared on 64 sampled
+    # tokens; the five workloads are compared over their whole batches.
     c = small_moe_case(1024, 128, 192, 64, 8, 4, 16, adapters="zipf", routing="zipf")
     d = make_moe_case(c, seed=6, device=DEV)
     rng = np.random.default_rng(3)
@@ -243,6 +285,8 @@ def test_forward_many_experts_top8():
 def test_forward_maximum_bins_and_top32():
     """The largest expert x adapter table (E = 1024, L = 10: 11264 bins) and
     the largest top-k the router kernel takes (k = 32)."""
+    # (compared on sampled tokens for the reason given in the top-8 test: a
+    # Zipf-routed output at 8.6 x RMS sits one bf16 half-ulp from the bound)
     c = small_moe_case(1500, 64, 128, 1024, 4, 10, 16, routing="zipf")
     d = make_moe_case(c, seed=12, device=DEV)
     rng = np.random.default_rng(12)
@@ -359,8 +403,7 @@ def test_two_phase_launch_equals_two_launches(monkeypatch, name):
     assert "gemm_gate_up_down" in names["2"] and "gemm_gate_up_down" not in names["1"], names
     assert torch.equal(outs["1"], outs["2"])
     n = np_inputs(d, lazy=True)
-    tokens = np.arange(min(d["x"].shape[0], 16))
-    ok, msg = compare(outs["2"][torch.as_tensor(tokens, device=DEV)], _oracle_forward(n, tokens), name)
+    ok, msg = compare(outs["2"], _oracle_forward(n), name)
     assert ok, msg
 
 
@@ -431,14 +474,14 @@ def test_linear_dense(T, tuned):
         torch.cuda.synchronize()
     finally:
         binding.moelora_load_tuning(None)
-    tokens = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(2).choice(T, 16, replace=False))
-    x = np_inputs({"x": d["x"]})["x"][tokens]
-    lo = d["lora_ids"].cpu().numpy()[tokens]
-    W = np_inputs({"W": d["W"]})["W"]
-    A = np_inputs({"A": d["A"]})["A"]
-    B = np_inputs({"B": d["B"]})["B"]
-    exp = ref.moe_lora_linear_ref(x, lo, W, A, B)
-    ok, msg = compare(out[torch.as_tensor(tokens, device=DEV)], exp, f"dense T={T}")
+    # every token of the batch against the oracle
+    key = f"dense_t{T}"
+    if key not in _ORACLE:
+        n = np_inputs({k: d[k] for k in ("x", "W", "A", "B")})
+        _ORACLE[key] = ref.moe_lora_linear_ref(n["x"], d["lora_ids"].cpu().numpy(), n["W"], n["A"],
+                                               n["B"])
+    ok, msg = compare(out, _ORACLE[key], f"dense T={T} ({'tuned' if tuned else 'built-in'})")
+    print(msg)
     assert ok, msg
 
 
@@ -452,8 +495,8 @@ def test_forward_dense_mlp(T, tuned):
     d = make_moe_case(CONFIGS[f"dense_mlp_t{T}"], seed=0, device=DEV)
     binding.moelora_load_tuning(table if tuned else None)
     try:
-        tokens = np.arange(T) if T <= 8 else np.sort(np.random.default_rng(3).choice(T, 8, replace=False))
-        _run_parity(d, tokens=tokens, what=f"dense MLP T={T}")
+        _run_parity(d, what=f"dense MLP T={T} ({'tuned' if tuned else 'built-in'})",
+                    key=f"dense_mlp_t{T}")
     finally:
         binding.moelora_load_tuning(None)
 
