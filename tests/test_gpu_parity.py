@@ -501,6 +501,43 @@ def test_forward_dense_mlp(T, tuned):
         binding.moelora_load_tuning(None)
 
 
+@pytest.mark.parametrize("T", [12, 100, 700])
+def test_forward_off_ladder_batch_sizes_under_the_tuned_table(T):
+    """Batch sizes that the tuning sweep did not sample take the choice of
+    their batch-size bucket in the shipped table; compared in full."""
+    import dataclasses
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    base = CONFIGS["prefill"] if T >= 512 else CONFIGS["decode"]
+    c = dataclasses.replace(base, name=f"decode_shapes_t{T}", T=T)
+    d = make_moe_case(c, seed=4, device=DEV)
+    binding.moelora_load_tuning(table)
+    try:
+        _run_parity(d, what=f"decode shapes T={T} (tuned bucket)")
+    finally:
+        binding.moelora_load_tuning(None)
+
+
+@pytest.mark.parametrize("T", [3, 24, 200])
+def test_linear_off_ladder_batch_sizes_under_the_tuned_table(T):
+    import dataclasses
+    import os
+    table = os.path.join(os.path.dirname(binding.__file__), "tuning")
+    c = dataclasses.replace(CONFIGS["dense_t1"], name=f"dense_t{T}", T=T)
+    d = make_linear_case(c, seed=4, device=DEV)
+    binding.moelora_load_tuning(table)
+    try:
+        out = binding.moe_lora_linear(d["x"], d["lora_ids"], d["W"], d["A"], d["B"])
+        torch.cuda.synchronize()
+    finally:
+        binding.moelora_load_tuning(None)
+    n = np_inputs({k: d[k] for k in ("x", "W", "A", "B")})
+    exp = ref.moe_lora_linear_ref(n["x"], d["lora_ids"].cpu().numpy(), n["W"], n["A"], n["B"])
+    ok, msg = compare(out, exp, f"dense T={T} (tuned bucket)")
+    print(msg)
+    assert ok, msg
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_linear_random_shapes(seed):
     # seeded random dense multi-LoRA linears: ragged T, K and N off the tile

@@ -85,3 +85,31 @@ def test_shipped_table_parses():
         pytest.skip("no shipped table")
     binding.moelora_load_tuning(path)
     assert binding.moelora_tuning_entries() > 0
+
+
+def test_sweep_buckets_cover_every_batch_size():
+    from lora_mixture_experts_gb300 import tune
+    for fam in tune.FAMILIES.values():
+        b = tune.buckets(fam.ladder)
+        assert b[0][0] == 1 and b[-1][1] == tune.T_MAX
+        for (lo, hi), t in zip(b, fam.ladder):
+            assert lo <= t <= hi                      # each sampled size sits in its own bucket
+        for (_, hi), (lo, _) in zip(b, b[1:]):
+            assert lo == hi + 1                       # no gaps, no overlaps
+
+
+def test_sweep_lines_merge_buckets_and_load(tmp_path):
+    from lora_mixture_experts_gb300 import tune
+    key = "moe T=@ k=4 E=32 H=2880 I=2880 L=8 r=32"
+    picks = [(1, 1, "tn=16 ksplit=2 phases=2"), (2, 2, "tn=16 ksplit=2 phases=2"),
+             (3, 5, None), (6, 11, "tn=32 ksplit=1 phases=2"), (12, tune.T_MAX, "tn=256 ksplit=1")]
+    lines = tune.merge_lines(key, picks)
+    assert lines == ["moe T=1-2 k=4 E=32 H=2880 I=2880 L=8 r=32 tn=16 ksplit=2 phases=2",
+                     "moe T=6-11 k=4 E=32 H=2880 I=2880 L=8 r=32 tn=32 ksplit=1 phases=2",
+                     f"moe T=12-{tune.T_MAX} k=4 E=32 H=2880 I=2880 L=8 r=32 tn=256 ksplit=1"]
+    binding.moelora_load_tuning(_write(tmp_path, "s.cfg", "\n".join(lines) + "\n"))
+    assert binding.moelora_tuning_entries() == 3
+    # T = 4 falls in the built-in bucket, T = 8 (off the ladder) in the tn=32 one
+    base = binding.moelora_workspace_bytes(moelora_dims(8, 4, 32, 2880, 2880, 8, 32))
+    binding.moelora_load_tuning(None)
+    assert binding.moelora_workspace_bytes(moelora_dims(8, 4, 32, 2880, 2880, 8, 32)) != base
