@@ -442,7 +442,9 @@ def measure(case, args, steps, warmup, rank, world, device, peaks, sampler, e2e=
     for i in range(K):
         for j in range(nl):
             per.setdefault(names[j], []).append(ev[i][j].elapsed_time(ev[i][j + 1]))
-    kernel_ms = {n: sum(v) / len(v) for n, v in per.items()}
+    # median over the steps: a step that the host delayed (events recorded
+    # late) does not move the kernel's figure
+    kernel_ms = {n: statistics.median(v) for n, v in per.items()}
     dom = max(kernel_work, key=lambda n: kernel_ms.get(n, 0.0))
     w = kernel_work[dom]
     region_s = K * ms / 1e3

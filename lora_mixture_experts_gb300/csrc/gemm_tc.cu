@@ -39,11 +39,14 @@
 //
 // Shrink items precede main items in the item order and a main item's
 // producer waits (bounded) for its tile's shrink items before loading the
-// z chunks.  Every CTA (pair) of the persistent grid is resident at once
-// (grid <= what fits, one CTA per SM), so the wait always ends.
+// z chunks.  Items are claimed in index order from a counter by CTAs (CTA
+// pairs) that are running, so every item waited for was claimed earlier by a
+// running CTA and the wait ends even when only part of the grid is resident
+// (another stream's kernels holding SMs).
 #include "gemm_tc.cuh"
 
 #include <algorithm>
+#include <cstddef>
 
 namespace moelora {
 namespace {
@@ -76,7 +79,10 @@ struct Cfg {
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5 + 3 * kQ;
   static constexpr int kRingOff = kBarOff + kNumBars * 8 + 16;   // RingEntry[kQ]
-  static constexpr int kSmemBytes = 1024 + kRingOff + kQ * static_cast<int>(sizeof(RingEntry));
+  // the producer's per-stage copy accounting (4 x kStages ints), see the end
+  // of gemm_body
+  static constexpr int kAcctOff = kRingOff + kQ * static_cast<int>(sizeof(RingEntry));
+  static constexpr int kSmemBytes = 1024 + kAcctOff + 4 * kStages * 4 + 16;
   static constexpr int kMRows = PAIR ? 256 : 128;   // weight rows of one item
   // shared-memory offset of K block j's A / B tile inside a stage
   __host__ __device__ static constexpr int a_off(int j) { return j * kATileBytes; }
@@ -174,8 +180,9 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
 // layer (NPH = 2: gate_up items, then down items, in one item order with one
 // claim counter).  A down item of a two-phase launch waits for its token
 // tile's activation rows: every gate_up main item of the tile counts on the
-// tile's counter once its rows are stored.  Items are claimed in order and
-// every CTA is resident, so the wait ends.  NPH is a template argument so
+// tile's counter once its rows are stored.  Items are claimed in order by
+// running CTAs, so the gate_up items waited for were claimed earlier by
+// running CTAs and the wait ends.  NPH is a template argument so
 // that the one-phase kernel reads its parameters at fixed offsets.
 template <int TN, bool PAIR, int NPH>
 __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps& maps1,
@@ -199,14 +206,20 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   RingEntry* ring = reinterpret_cast<RingEntry*>(smem + C::kRingOff);
+  // Per stage slot, what the producer thread of this CTA issued into its
+  // latest use (stage count, or -1, and bytes) and, on the CTA that counts a
+  // stage's bytes (the leader), what it posted on the slot's full barrier.
+  int* st_gen = reinterpret_cast<int*>(smem + C::kAcctOff);
+  int* st_bytes = st_gen + C::kStages;
+  int* po_gen = st_gen + 2 * C::kStages;
+  int* po_bytes = st_gen + 3 * C::kStages;
+  int* peer_abort = st_gen + 4 * C::kStages;   // the peer CTA's abort flag, copied at the end
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // CTA pairs: rank 0 leads; items are shared by the two CTAs of a cluster
   const uint32_t rank = PAIR ? cluster_rank() : 0;
   const bool leader = rank == 0;
-  const int unit = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
-  const int n_units = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -218,12 +231,21 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
       mbar_init(smem_u32(&acce_bar[b]), PAIR ? 8 : 4);   // epilogue warps of both CTAs
     }
     mbar_init(smem_u32(drain_bar), 1);
-    // consumers of a ring entry: producer, MMA issuer (leader only), four epilogue warps
+    // consumers of a ring entry: producer, MMA issuer (leader only), four
+    // epilogue warps; on CTA pairs the peer's five release the leader's
+    // entry barrier too (the leader's scheduler writes both rings)
     for (int q = 0; q < kQ; ++q) {
       mbar_init(smem_u32(&itemf_bar[q]), 1);
-      mbar_init(smem_u32(&iteme_bar[q]), leader ? 6 : 5);
+      mbar_init(smem_u32(&iteme_bar[q]), PAIR ? (leader ? 11 : 1) : 6);
       mbar_init(smem_u32(&itemp_bar[q]), 1);
     }
+    for (int st = 0; st < C::kStages; ++st) {
+      st_gen[st] = -1;
+      st_bytes[st] = 0;
+      po_gen[st] = -1;
+      po_bytes[st] = 0;
+    }
+    *peer_abort = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -268,15 +290,31 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
   // shrink completions a tile's item waits for: every CTA of the item signals
   const int done_scale = PAIR ? 2 : 1;
 
+  // Ring entries: on CTA pairs the leader writes the peer's entries too, so
+  // the peer's consumers wait on "written" with a cluster-scope acquire and
+  // release an entry on the leader's barrier (remotely); the leader's own
+  // consumers keep CTA-scope waits and arrives, which cost less per item.
+  const bool remote_ring = PAIR && !leader;
+  const uint32_t iteme_rel0 = remote_ring ? mapa_shared(smem_u32(&iteme_bar[0]), 0) : 0;
+  auto entry_written = [&](int q, uint32_t parity) -> bool {
+    return remote_ring ? mbar_wait_cluster(smem_u32(&itemf_bar[q]), parity, abort_flag)
+                       : mbar_wait(smem_u32(&itemf_bar[q]), parity, abort_flag);
+  };
+  auto entry_release = [&](int q) {
+    if (remote_ring)
+      mbar_arrive_cluster(iteme_rel0 + q * 8);
+    else
+      mbar_arrive(smem_u32(&iteme_bar[q]));
+  };
   // Consume ring entry qc (single-thread consumers: producer, MMA issuer):
   // wait until it is written, copy it, release the slot.
   auto ring_take = [&](uint32_t qc, int& w, TileInfo& ti, bool producer) -> bool {
     const int q = static_cast<int>(qc % kQ);
-    if (!mbar_wait(smem_u32(&itemf_bar[q]), (qc / kQ) & 1, abort_flag)) return false;
+    if (!entry_written(q, (qc / kQ) & 1)) return false;
     w = ring[q].w;
     ti = ring[q].ti;
-    mbar_arrive(smem_u32(&iteme_bar[q]));
-    if (producer) mbar_arrive(smem_u32(&itemp_bar[q]));
+    entry_release(q);
+    if (producer && leader) mbar_arrive(smem_u32(&itemp_bar[q]));
     return true;
   };
 
@@ -285,20 +323,39 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
     if (lane == 0) {
       uint32_t cnt = 0;
       bool ok = true;
-      // one TMA load into this CTA's shared memory, counted on the leader's
-      // full barrier when paired
-      auto load2 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y) {
+      // one TMA load of `bytes` into the current stage of this CTA's shared
+      // memory, counted on the leader's full barrier when paired; the bytes
+      // add up in `stage_bytes` and go to the stage's accounting once the
+      // stage is issued (for an exact wind-down after an abort)
+      int stage_bytes = 0;
+      auto load2 = [&](uint32_t bytes, uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y) {
+        stage_bytes += static_cast<int>(bytes);
         if (PAIR) tma_load_2d_pair(dst, m, fb, x, y); else tma_load_2d(dst, m, fb, x, y);
       };
-      auto load3 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z) {
+      auto load3 = [&](uint32_t bytes, uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y,
+                       int z) {
+        stage_bytes += static_cast<int>(bytes);
         if (PAIR) tma_load_3d_pair(dst, m, fb, x, y, z); else tma_load_3d(dst, m, fb, x, y, z);
       };
-      auto load4 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z, int w) {
+      auto load4 = [&](uint32_t bytes, uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y,
+                       int z, int w) {
+        stage_bytes += static_cast<int>(bytes);
         if (PAIR) tma_load_4d_pair(dst, m, fb, x, y, z, w); else tma_load_4d(dst, m, fb, x, y, z, w);
       };
-      auto load5 = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y, int z, int w,
-                       int v) {
+      auto load5 = [&](uint32_t bytes, uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y,
+                       int z, int w, int v) {
+        stage_bytes += static_cast<int>(bytes);
         if (PAIR) tma_load_5d_pair(dst, m, fb, x, y, z, w, v); else tma_load_5d(dst, m, fb, x, y, z, w, v);
+      };
+      auto stage_issued = [&](int s) {
+        st_bytes[s] = stage_bytes;
+        stage_bytes = 0;
+      };
+      // the leader's byte count of stage s for this use of it
+      auto post = [&](int s, uint32_t bytes) {
+        po_gen[s] = static_cast<int>(cnt);
+        po_bytes[s] = static_cast<int>(bytes);
+        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), bytes);
       };
       // Deferred token rows.  Before the grid dependency wait (first item,
       // unpaired tiles), or before its tile's activations are complete (a
@@ -313,8 +370,8 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
       const int* defer_cnt = nullptr;   // NULL: wait for the preceding launch
       int defer_target = 0;
       bool defer_ok = true;
-      auto load_deferred_rows = [&](int nkc, int kc0, int rot, const CUtensorMap* tb,
-                                    int brow0) -> bool {
+      auto load_deferred_rows = [&](int nkc, int kc0, int rot, const CUtensorMap* tb, int brow0,
+                                    int brows) -> bool {
         if (defer_cnt) {
           const uint64_t t0 = globaltimer_ns();
           while (ld_acquire_gpu(defer_cnt) < defer_target) {
@@ -337,7 +394,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             for (int j = 0; j < C::kKB && d * C::kKB + j < nkc; ++j) {
               const int i = d * C::kKB + j;
               const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
-              load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+              st_bytes[s] += brows * 128;   // (a stage issued earlier)
+              if (PAIR) tma_load_2d_pair(st + C::b_off(j), tb, fb, kc * 64, brow0);
+              else tma_load_2d(st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
           }
         }
@@ -351,6 +410,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             !mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, abort_flag))
           return false;
         fb = PAIR ? mapa_shared(smem_u32(&full_bar[s]), 0) : smem_u32(&full_bar[s]);
+        st_gen[s] = static_cast<int>(cnt);
         return true;
       };
       // stage and phase of stage count cnt, kept running (no division)
@@ -421,22 +481,23 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             uint32_t fb;
             if (!(ok = acquire(s, sph, fb))) break;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-            if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
+            if (leader) post(s, nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
               const int kc = kb0 + j;
               if (a_run >= 0) {
-                load4(st + C::a_off(j), &maps.la_run, fb, kc * 64, 0, ti.expert, a_run);
+                load4(spc * p.r * 128, st + C::a_off(j), &maps.la_run, fb, kc * 64, 0, ti.expert, a_run);
               } else {
                 for (int q = 0; q < ns_me; ++q)
-                  load4(st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
+                  load4(p.r * 128, st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
                         p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
               }
-              if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+              if (waited) load2(brows * 128, st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
-            if (!waited && ++n_def == C::kStages && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0))
+            stage_issued(s);
+            if (!waited && ++n_def == C::kStages && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0, brows))
               ok = false;
           }
-          if (ok && !waited && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0)) ok = false;
+          if (ok && !waited && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0, brows)) ok = false;
         } else {
           const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
           const int kc0 = p.split_k0[it.ks];
@@ -454,20 +515,21 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             uint32_t fb;
             if (!(ok = acquire(s, sph, fb))) break;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-            if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nkb * per_kb);
+            if (leader) post(s, nkb * per_kb);
             for (int j = 0; j < nkb; ++j) {
               const int i = i0 + j;
               const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
               if (gate_up)   // 64 features, each gate row followed by its up row, in one box
-                load4(st + C::a_off(j), &maps.w, fb, kc * 64, 0, grow, ti.expert);
+                load4(kATileBytes, st + C::a_off(j), &maps.w, fb, kc * 64, 0, grow, ti.expert);
               else
-                load3(st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
-              if (waited) load2(st + C::b_off(j), tb, fb, kc * 64, brow0);
+                load3(kATileBytes, st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
+              if (waited) load2(brows * 128, st + C::b_off(j), tb, fb, kc * 64, brow0);
             }
-            if (!waited && ++n_def == C::kStages && !load_deferred_rows(nkc, kc0, rot, tb, brow0))
+            stage_issued(s);
+            if (!waited && ++n_def == C::kStages && !load_deferred_rows(nkc, kc0, rot, tb, brow0, brows))
               ok = false;
           }
-          if (ok && !waited && !load_deferred_rows(nkc, kc0, rot, tb, brow0)) ok = false;
+          if (ok && !waited && !load_deferred_rows(nkc, kc0, rot, tb, brow0, brows)) ok = false;
           if (ok && p.r > 0 && ti.nslots > 0 && it.ks == p.ksplit - 1) {
             // the tile's shrink results must be complete and visible to TMA
             const int target = p.done_target * ti.nsh * done_scale;
@@ -493,7 +555,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
               uint32_t fb;
               if (!(ok = acquire(s, sph, fb))) break;
               const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-              if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), nsub * per_sub);
+              if (leader) post(s, nsub * per_sub);
               for (int j = 0; j < nsub; ++j) {
                 const int per_slot = p.lora_chunks * p.z_parts;
                 const int sl = (i0 + j) / per_slot;
@@ -506,32 +568,22 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
                     MOELORA_IN_RANGE(p.err, ti.slot_base + sl, 0, p.zpart_slots) ? ti.slot_base + sl : 0;
                 const int a = p.slot_adapter[sidx_ok];
                 if (gate_up)
-                  load5(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, 0, grow, ti.expert, a);
+                  load5(128 * lw * 2, st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, 0, grow, ti.expert,
+                        a);
                 else
-                  load4(st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, ti.expert, a);
-                load2(st + C::lora_b_off(j, lw), tz, fb, part * p.r + c * lw,
+                  load4(128 * lw * 2, st + C::lora_a_off(j, lw), &maps.lb, fb, c * lw, grow, ti.expert, a);
+                load2(brows * lw * 2, st + C::lora_b_off(j, lw), tz, fb, part * p.r + c * lw,
                       (ti.slot_base + sl) * TN + static_cast<int>(rank) * nh);
               }
+              stage_issued(s);
             }
           }
         }
       }
       if (!ok) {
+        // (the copies already issued are waited for at the end of the kernel)
         *abort_flag = 1;
         flag_error(p.err, kStatusTimeout);
-        // let the copies already issued land before the CTA exits
-        if (PAIR) {
-          // (their completions count on the leader's barriers: give them time)
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
-        } else {
-          const uint32_t first = cnt > (uint32_t)C::kStages ? cnt - C::kStages : 0;
-          for (uint32_t c = first; c < cnt; ++c) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(smem_u32(&full_bar[c % C::kStages]), (c / C::kStages) & 1))
-              if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-          }
-        }
       }
     }
   } else if (warp == 1) {
@@ -654,36 +706,53 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
     }
   } else if (warp == kSchedWarp) {
     // ------------------------------------------------------------ item scheduler
-    // Writes the CTA's item sequence into the ring.  Unpaired tiles claim
-    // items from the launch's counter as they go: items cost about the same,
-    // but SMs stream from HBM at different rates, and a fixed share leaves
-    // the slowest SMs the tail (decode 0.266 -> 0.261 ms, dense T=1 0.103 ->
-    // 0.094 ms on GB300).  Paired tiles keep the fixed round-robin share,
-    // computed by each CTA of the pair alike: claiming for both CTAs from the
-    // leader (writing the peer's ring remotely) measured no faster there.
-    // Items are claimed in index order, so shrink items are always claimed
-    // before the main items that wait for them.
-    if (lane == 0) {
-      const bool dyn = !PAIR && p.work_ctr != nullptr;
+    // Writes the CTA's item sequence into the ring, claiming items from the
+    // launch's counter as it goes: items cost about the same, but SMs stream
+    // from HBM at different rates, and a fixed share leaves the slowest SMs
+    // the tail (decode 0.266 -> 0.261 ms, dense T=1 0.103 -> 0.094 ms on
+    // GB300).  On CTA pairs the leader claims for the pair and writes the
+    // peer's ring entry as well (the peer's scheduler has nothing to do).
+    // Items are claimed in index order by CTAs that are running, so shrink
+    // items are always claimed, and finished, by resident CTAs before any
+    // main item that waits for them: no wait depends on a CTA (pair) that
+    // has not started, however many of the grid's CTAs are resident.
+    if (lane == 0 && leader) {
       bool ok = true;
+      const uint32_t peer_ring = PAIR ? mapa_shared(smem_u32(ring), 1) : 0;
+      const uint32_t peer_itemf = PAIR ? mapa_shared(smem_u32(&itemf_bar[0]), 1) : 0;
       for (uint32_t qp = 0;; ++qp) {
         const int q = static_cast<int>(qp % kQ);
-        if (!(ok = mbar_wait(smem_u32(&iteme_bar[q]), ((qp / kQ) & 1) ^ 1, abort_flag))) break;
+        // every consumer (of both CTAs) has read the entry's previous use
+        if (!(ok = PAIR ? mbar_wait_cluster(smem_u32(&iteme_bar[q]), ((qp / kQ) & 1) ^ 1, abort_flag)
+                        : mbar_wait(smem_u32(&iteme_bar[q]), ((qp / kQ) & 1) ^ 1, abort_flag)))
+          break;
         // claim no further ahead than kClaimAhead items past the producer, so
         // that the items left go to whichever CTA runs out first
         if (qp >= static_cast<uint32_t>(kClaimAhead)) {
           const uint32_t e = qp - kClaimAhead;
           if (!(ok = mbar_wait(smem_u32(&itemp_bar[e % kQ]), (e / kQ) & 1, abort_flag))) break;
         }
-        int w = dyn ? atomicAdd(p.work_ctr, 1) : unit + static_cast<int>(qp) * n_units;
+        int w = atomicAdd(p.work_ctr, 1);
         if (w >= n_items) w = -1;
+        TileInfo ti = {};
         if (w >= 0) {
           const bool w1 = NPH == 2 && w >= items0;
           const GemmParams& pw = w1 ? p1 : p0;
-          ring[q].ti = p.tiles[decode_item(w - (w1 ? items0 : 0), n_sh, n_tiles, pw.n_mtiles,
-                                           pw.group_tiles, p.shrink).tile];
+          ti = p.tiles[decode_item(w - (w1 ? items0 : 0), n_sh, n_tiles, pw.n_mtiles, pw.group_tiles,
+                                   p.shrink).tile];
         }
+        ring[q].ti = ti;
         ring[q].w = w;
+        if (PAIR) {
+          // the peer's copy of the entry, released by its "written" arrive
+          const uint32_t dst = peer_ring + q * static_cast<uint32_t>(sizeof(RingEntry));
+          st_cluster_u32(dst, static_cast<uint32_t>(w));
+          const uint32_t* tv = reinterpret_cast<const uint32_t*>(&ti);
+#pragma unroll
+          for (int i = 0; i < static_cast<int>(sizeof(TileInfo) / 4); ++i)
+            st_cluster_u32(dst + static_cast<uint32_t>(offsetof(RingEntry, ti)) + 4 * i, tv[i]);
+          mbar_arrive_cluster(peer_itemf + q * 8);
+        }
         mbar_arrive(smem_u32(&itemf_bar[q]));
         if (w < 0) break;
       }
@@ -703,7 +772,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
       // the next ring entry: every epilogue thread reads it, the warps agree
       // on the outcome of the wait, and each warp releases the slot
       const int q = static_cast<int>(qc % kQ);
-      const bool got = mbar_wait(smem_u32(&itemf_bar[q]), (qc / kQ) & 1, abort_flag);
+      const bool got = entry_written(q, (qc / kQ) & 1);
       if (bar_red_or(1, 128, !got || *abort_flag)) {
         if (!got) flag_error(p.err, kStatusTimeout);
         *abort_flag = 1;
@@ -712,7 +781,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
       const int w = ring[q].w;
       const TileInfo ti = ring[q].ti;
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&iteme_bar[q]));
+      if (lane == 0) entry_release(q);
       if (w < 0) break;
       const int ph = NPH == 2 && w >= items0 ? 1 : 0;
       const GemmParams& p = NPH == 2 && ph ? p1 : p0;
@@ -901,7 +970,44 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
   }
 
   __syncthreads();
+  // (each CTA of a pair hands its abort flag to the other, so that both take
+  // the same decision below)
+  if (PAIR && threadIdx.x == 0)
+    st_cluster_u32(mapa_shared(smem_u32(peer_abort), rank ^ 1), static_cast<uint32_t>(*abort_flag));
   if (PAIR) cluster_sync();   // no CTA leaves while its peer may still touch it
+  const bool any_abort = *abort_flag || (PAIR && *reinterpret_cast<volatile int*>(peer_abort));
+  // After an abort some copies may still be in flight into a stage whose
+  // MMAs never ran.  Every producer has stopped issuing by now, and its
+  // accounting says, per stage slot, what it last posted and issued: the CTA
+  // that counts a slot's bytes (the leader; each CTA when unpaired) settles
+  // the slot's latest phase -- posts the bytes nobody announced, or marks as
+  // arrived the announced bytes nobody sent -- and waits (bounded) until the
+  // copies actually issued have landed.  Nothing then writes into a CTA's
+  // shared memory or barriers after it exits.
+  if (warp == 0 && lane == 0 && leader) {
+    if (any_abort) {
+      for (int s = 0; s < C::kStages; ++s) {
+        const int g_me = st_gen[s];
+        const int b_me = st_bytes[s];
+        const int g_pe = PAIR ? static_cast<int>(ld_cluster_u32(mapa_shared(smem_u32(&st_gen[s]), 1))) : -1;
+        const int b_pe = PAIR ? static_cast<int>(ld_cluster_u32(mapa_shared(smem_u32(&st_bytes[s]), 1))) : 0;
+        const int g = max(max(g_me, g_pe), po_gen[s]);
+        if (g < 0) continue;
+        const int arrived = (g_me == g ? b_me : 0) + (g_pe == g ? b_pe : 0);
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        if (po_gen[s] == g) {
+          if (po_bytes[s] > arrived) mbar_complete_tx(fb, static_cast<uint32_t>(po_bytes[s] - arrived));
+        } else {
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(arrived));
+        }
+        const uint32_t parity = (static_cast<uint32_t>(g) / C::kStages) & 1;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(fb, parity))
+          if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      }
+    }
+  }
+  if (PAIR && any_abort) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     if (PAIR)
@@ -979,7 +1085,8 @@ cudaError_t launch_tn(const GemmMaps& maps0, const GemmParams& p0, const GemmMap
     if (max_units < 1) return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
-  // every CTA (pair) must be resident at once: items wait on one another
+  // no more CTAs (pairs) than fit at once: a persistent CTA beyond that
+  // would only start when another ends
   const int units = std::max(1, std::min(grid, max_units));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(PAIR ? 2 * units : units);
