@@ -17,7 +17,8 @@ counts.  Rank 0 prints one JSON line.
 
 With the decode batch as the headline (the default), one GPU, the other
 workloads (prefill, skewed, the dense linear and the dense MLP at T = 1, 8,
-64, 512) are timed after it, about a quarter second each, and reported under
+64, 512, and the merged-weight fast path on the decode and skewed layers)
+are timed after it, about a quarter second each, and reported under
 `per_config` with their own roofline, clocks and parity.  Every timed
 output is compared with the oracle over its whole batch (`parity`).
 
@@ -519,10 +520,90 @@ def measure(case, args, steps, warmup, rank, world, device, peaks, sampler, e2e=
     return res, out, d
 
 
+def merge_parity(d, Wgu, Wd, a, experts):
+    """The merged weights of `experts` against float64 W + B A of adapter a
+    (one bf16 rounding allowed: |got - exact| <= 2^-8 |exact| + 1e-6)."""
+    import numpy as np
+    from oracle import moe_lora_ref as ref
+    from lora_mixture_experts_gb300.inputs import bf16_bits
+    worst = 0.0
+    for e in experts:
+        for W, B, A, got in ((d["W_gate_up"], d["B_gu"], d["A_gu"], Wgu), (d["W_down"], d["B_d"], d["A_d"], Wd)):
+            exact = ref.as_f64(bf16_bits(W[e])) + ref.as_f64(bf16_bits(B[a, e])) @ ref.as_f64(bf16_bits(A[a, e]))
+            g = ref.as_f64(bf16_bits(got[e]))
+            worst = max(worst, float(np.max(np.abs(g - exact) / (2.0 ** -8 * np.abs(exact) + 1e-6))))
+    return {"experts": len(experts), "worst_error_over_bound": worst, "pass": bool(worst <= 1.0)}
+
+
+def measure_merge(case, peaks, sampler, target_s=0.25):
+    """The merged-weight fast path (moe_lora_merge_adapter) on a workload's
+    layer: one call merges one adapter into both projections of every
+    expert.  HBM-bound: the bytes of merge_work per call."""
+    import torch
+    from lora_mixture_experts_gb300 import binding, roofline
+    from lora_mixture_experts_gb300.inputs import make_moe_case
+    d = make_moe_case(case, seed=0, device="cuda")
+    a = case.L - 1
+    Wgu = torch.empty_like(d["W_gate_up"])
+    Wd = torch.empty_like(d["W_down"])
+
+    def call():
+        binding.moe_lora_merge_adapter(a, d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"], d["A_d"],
+                                       d["B_d"], W_gate_up_out=Wgu, W_down_out=Wd)
+    call()
+    torch.cuda.synchronize()
+    names = binding.moelora_last_launches()
+    for _ in range(3):
+        call()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    call()
+    e1.record()
+    torch.cuda.synchronize()
+    K = int(min(2000, max(20, target_s * 1e3 / e0.elapsed_time(e1))))
+    t0 = time.time()
+    e0.record()
+    for _ in range(K):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    for i in range(K):
+        binding.moelora_set_timing_events(ev[i])
+        call()
+    torch.cuda.synchronize()
+    binding.moelora_set_timing_events(None)
+    clocks = sampler.summary(t0, time.time())
+    kernel_ms = {n: statistics.median([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)])
+                 for j, n in enumerate(names)}
+    E, H, I, r = case.E, case.H, case.I, case.r
+    gu_bytes = 2 * E * 2 * I * H * 2 + E * (r * H + 2 * I * r) * 2
+    achieved = gu_bytes / (kernel_ms["merge_gate_up"] / 1e3) / 1e9
+    w = roofline.merge_work(E, H, I, r)
+    experts = list(range(E)) if E * (3 * I * H) <= 1 << 30 else list(range(0, E, max(1, E // 4)))[:4]
+    res = {
+        "workload": f"merge of one adapter into {case.name}'s layer: E={E}, H={H}, I={I}, r={r}",
+        "ms_per_step": ms, "steps": K, "unit": "ms per merge",
+        "roofline": {"kernel": "merge_gate_up", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": f"{peaks['source']} (HBM copy)", "algorithmic_bytes": gu_bytes,
+                     "kernel_ms": kernel_ms["merge_gate_up"], "traffic": load_traffic(f"merge_{case.name}", "merge_gate_up")},
+        "layer_roofline": {"bound": "hbm", "t_roof_ms": 1e3 * w.bytes / (peaks["hbm_gbs"] * 1e9),
+                           "frac": 1e3 * w.bytes / (peaks["hbm_gbs"] * 1e9) / ms, "bytes": w.bytes, "flops": w.flops},
+        "kernel_ms": kernel_ms, "gpu_launches": len(names) * K, "clocks": clocks,
+        "parity": merge_parity(d, Wgu, Wd, a, experts),
+    }
+    del d, Wgu, Wd
+    return res
+
+
 # the workloads timed after the headline in a default run (each one's own
 # line under `per_config`); the headline stays the decode batch
 PER_CONFIG = ("prefill", "skewed", "dense_t1", "dense_t8", "dense_t64", "dense_t512",
-              "dense_mlp_t1", "dense_mlp_t8", "dense_mlp_t64", "dense_mlp_t512")
+              "dense_mlp_t1", "dense_mlp_t8", "dense_mlp_t64", "dense_mlp_t512",
+              "merge_decode", "merge_skewed")
 
 
 def run_ours(args, rank, world, device):
@@ -570,8 +651,11 @@ def run_ours(args, rank, world, device):
         if world == 1 and per_names:
             res["per_config"] = {}
             for name in per_names:
-                c = CONFIGS[name]
                 torch.cuda.empty_cache()
+                if name.startswith("merge_"):
+                    res["per_config"][name] = measure_merge(CONFIGS[name[len("merge_"):]], peaks, sampler)
+                    continue
+                c = CONFIGS[name]
                 # about a quarter second of timed calls
                 m, out, d = measure(c, args, None, max(args.warmup // 10, 5), rank, world, device, peaks,
                                     sampler)

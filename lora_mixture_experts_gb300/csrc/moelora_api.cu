@@ -1087,24 +1087,40 @@ int moe_lora_merge_adapter(const moelora_dims* d, int32_t adapter, const moelora
                            moelora_bf16* W_down_out, moelora_stream_t stream_) {
   if (!d || d->E < 1 || d->H < 8 || d->I < 8 || d->L < 1 || d->r < 1) return MOELORA_ERR_INVALID_ARG;
   if (adapter < 0 || adapter >= d->L) return MOELORA_ERR_INVALID_ARG;
-  if (d->r > 128) return MOELORA_ERR_UNSUPPORTED;
+  if (!lora_rank_ok(d->r) || d->H % 8 || d->I % 8) return MOELORA_ERR_UNSUPPORTED;
   if (!W_gate_up || !W_down || !A_gu || !B_gu || !A_d || !B_d || !W_gate_up_out || !W_down_out)
     return MOELORA_ERR_INVALID_ARG;
+  const void* ptrs[8] = {W_gate_up, W_down, A_gu, B_gu, A_d, B_d, W_gate_up_out, W_down_out};
+  for (const void* q : ptrs)
+    if (reinterpret_cast<uintptr_t>(q) % 16) return MOELORA_ERR_MISALIGNED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const size_t E = d->E, H = d->H, I = d->I, r = d->r, a = adapter;
   auto bf = [](const moelora_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); };
+  const uint32_t lw = lora_chunk_width(d->r);
+  const int sms = device_sms();
   Launcher ln(stream);
-  ln.before("merge_gate_up");
   // adapter a's [E][...] slices are contiguous in the [L][E][...] LoRA tensors
-  if (launch_merge(bf(W_gate_up), bf(B_gu) + a * E * 2 * I * r, bf(A_gu) + a * E * r * H,
-                   reinterpret_cast<__nv_bfloat16*>(W_gate_up_out), d->E, 2 * d->I, d->H, d->r,
-                   stream) != cudaSuccess)
-    return MOELORA_ERR_CUDA;
-  ln.before("merge_down");
-  if (launch_merge(bf(W_down), bf(B_d) + a * E * H * r, bf(A_d) + a * E * r * I,
-                   reinterpret_cast<__nv_bfloat16*>(W_down_out), d->E, d->H, d->I, d->r,
-                   stream) != cudaSuccess)
-    return MOELORA_ERR_CUDA;
+  struct Proj {
+    const char* name;
+    const moelora_bf16* W;
+    moelora_bf16* Wm;
+    const moelora_bf16* B;
+    const moelora_bf16* A;
+    size_t rows, cols;
+  };
+  const Proj proj[2] = {
+      {"merge_gate_up", W_gate_up, W_gate_up_out, B_gu + a * E * 2 * I * r, A_gu + a * E * r * H, 2 * I, H},
+      {"merge_down", W_down, W_down_out, B_d + a * E * H * r, A_d + a * E * r * I, H, I}};
+  for (const Proj& pj : proj) {
+    CUtensorMap mw, mwm, mb;
+    if (!enc3(&mw, pj.W, pj.cols, pj.rows, E, 64, 128) || !enc3(&mwm, pj.Wm, pj.cols, pj.rows, E, 64, 128) ||
+        !enc3(&mb, pj.B, r, pj.rows, E, lw, 128))
+      return MOELORA_ERR_CUDA;
+    ln.before(pj.name);
+    if (launch_merge(mw, mwm, mb, bf(pj.A), d->E, static_cast<int>(pj.rows), static_cast<int>(pj.cols),
+                     d->r, sms, stream) != cudaSuccess)
+      return MOELORA_ERR_CUDA;
+  }
   ln.finish();
   return MOELORA_OK;
 }

@@ -68,6 +68,15 @@ def linear_work(lora_ids, K, N, r):
     return Work(b, f)
 
 
+def merge_work(E, H, I, r):
+    """The merged-weight fast path for one adapter (W' = W + B A, both
+    projections): every base weight read once and its merged copy written
+    once, the adapter's A and B read once; 2r FLOP per merged element."""
+    w = E * (2 * I * H + H * I)
+    lora = E * (r * H + 2 * I * r + r * I + H * r)
+    return Work(2 * w * 2 + lora * 2, 2 * r * w)
+
+
 def load_peaks(root: str):
     """Measured peaks (copy bandwidth, cuBLAS bf16) if present, else the
     fallback figures of an earlier GB300 measurement."""

@@ -630,8 +630,12 @@ def test_forward_routed_large_batch():
 
 
 # ------------------------------------------------------------------ merged-weight fast path
-@pytest.mark.parametrize("shape", [(4, 136, 72, 3, 16), (2, 256, 512, 4, 64), (1, 264, 200, 2, 128)])
+@pytest.mark.parametrize("shape", [(4, 136, 72, 3, 16), (2, 256, 512, 4, 64), (1, 264, 200, 2, 128),
+                                   (3, 200, 136, 2, 48), (2, 1000, 712, 2, 96), (5, 128, 1224, 3, 32),
+                                   (2, 392, 264, 2, 80), (1, 136, 520, 1, 112)])
 def test_merge_adapter_weights(shape):
+    # ragged rows and columns (partial 128 x 128 tiles), several row ranges
+    # per column block, every chunk width of the rank (16, 32, 64)
     E, H, I, L, r = shape
     c = small_moe_case(8, H, I, E, 1, L, r)
     d = make_moe_case(c, seed=3, device=DEV)
@@ -648,6 +652,24 @@ def test_merge_adapter_weights(shape):
         g = got.float().cpu().numpy().astype(np.float64)
         # one bf16 rounding of the fp32 sum: within 2^-8 relative (+ a tiny absolute floor)
         assert np.all(np.abs(g - exp) <= 2.0 ** -8 * np.abs(exp) + 1e-6)
+
+
+@pytest.mark.parametrize("name", ["decode", "skewed"])
+def test_merge_adapter_weights_full_size(name):
+    """The merge at the bench workloads' layer sizes, every merged element of
+    a sample of experts against float64 W + B A (one bf16 rounding)."""
+    c = CONFIGS[name]
+    d = make_moe_case(c, seed=0, device=DEV)
+    a = c.L - 1
+    Wgu, Wd = binding.moe_lora_merge_adapter(a, d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"],
+                                             d["A_d"], d["B_d"])
+    torch.cuda.synchronize()
+    from lora_mixture_experts_gb300.inputs import bf16_bits
+    for e in (0, c.E // 2 + 1, c.E - 1):
+        for W, B, A, got in ((d["W_gate_up"], d["B_gu"], d["A_gu"], Wgu), (d["W_down"], d["B_d"], d["A_d"], Wd)):
+            exact = ref.as_f64(bf16_bits(W[e])) + ref.as_f64(bf16_bits(B[a, e])) @ ref.as_f64(bf16_bits(A[a, e]))
+            g = ref.as_f64(bf16_bits(got[e]))
+            assert np.all(np.abs(g - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-6), (name, e)
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode"])
