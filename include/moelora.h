@@ -250,9 +250,15 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x_dev,
  * Cited: the hybrid-attention decoder page, "static LoRA merge"
  * (merge_and_unload at initialisation removes the LoRA cost at run time), and
  * the multi-LoRA MoE blog's y = xW + xAB.
- *   d: E, H, I, L, r (T and k unused); 0 <= adapter < L; r <= 128.
+ *   d: E, H, I, L, r (T and k unused); 0 <= adapter < L; r a multiple of
+ *   16 up to 128 and H, I multiples of 8 (else MOELORA_ERR_UNSUPPORTED);
+ *   every pointer 16-byte aligned (else MOELORA_ERR_MISALIGNED).
  *   Outputs are caller-owned device buffers shaped like the inputs; they may
- *   not alias the inputs.  Run once per adapter switch; no workspace.
+ *   not alias the inputs.  Run once per adapter switch; no workspace.  The
+ *   rank-r products run on the tensor cores; the call moves each weight once
+ *   in and once out (HBM-bound).  Its waits are bounded like the layer's,
+ *   but with no workspace a wait that ran out cannot be reported (the merged
+ *   weights are then undefined); none of its waits depends on another CTA.
  */
 int moe_lora_merge_adapter(const moelora_dims* d, int32_t adapter,
                            const moelora_bf16* W_gate_up_dev, const moelora_bf16* W_down_dev,
