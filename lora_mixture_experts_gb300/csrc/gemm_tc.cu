@@ -64,17 +64,37 @@ struct RingEntry {
   int pad_[3];
   TileInfo ti;
 };
-constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
-
+// K-block width and pipeline shape of CTA-pair tiles (the tensor-bound
+// case): K blocks of MOELORA_PAIR_BK elements (64, or 32 with 64-byte rows),
+// MOELORA_PAIR_KB of them per stage, MOELORA_PAIR_STAGES stages.  Measured
+// on GB300 (same box): four stages of three 32-wide blocks (48 KB) against
+// three of two 64-wide blocks (64 KB): prefill 805 -> 885 us, dense T = 512
+// 188 -> 223 us, skewed 3.06 -> 3.28 ms; the 64-wide blocks stay.
+#ifndef MOELORA_PAIR_BK
+#define MOELORA_PAIR_BK 64
+#endif
+#ifndef MOELORA_PAIR_KB
+#define MOELORA_PAIR_KB 2
+#endif
+#ifndef MOELORA_PAIR_STAGES
+#define MOELORA_PAIR_STAGES 3
+#endif
 
 template <int TN, bool PAIR>
 struct Cfg {
+  // K-block width (elements): 64 (128-byte rows, 128-byte swizzle), or 32
+  // on CTA pairs (64-byte rows and swizzle)
+  static constexpr int kBK = PAIR ? MOELORA_PAIR_BK : 64;
+  static constexpr uint32_t kSwzK = kBK == 64 ? 2u : 4u;        // descriptor layout code
+  static constexpr uint32_t kSboK = 8u * kBK * 2u;                // bytes between 8-row groups
+  static constexpr int kATile = 128 * kBK * 2;                    // 128 weight rows of a K block
   static constexpr int kRowsB = PAIR ? TN / 2 : TN;   // token rows a CTA holds per K block
-  static constexpr int kKB = PAIR ? 2 : (TN <= 16 ? 4 : (TN <= 64 ? 2 : 1));   // K blocks per stage
-  static constexpr int kBTileBytes = kRowsB * 128;                  // per K block
-  static constexpr int kStageBytes = kKB * (kATileBytes + kBTileBytes);
+  static constexpr int kKB =
+      PAIR ? MOELORA_PAIR_KB : (TN <= 16 ? 4 : (TN <= 64 ? 2 : 1));   // K blocks per stage
+  static constexpr int kBTileBytes = kRowsB * kBK * 2;             // per K block
+  static constexpr int kStageBytes = kKB * (kATile + kBTileBytes);
   static constexpr int kStages =
-      PAIR ? 3 : (TN <= 16 ? 3 : (TN <= 32 ? 5 : (TN <= 64 ? 4 : (TN <= 128 ? 6 : 4))));
+      PAIR ? MOELORA_PAIR_STAGES : (TN <= 16 ? 3 : (TN <= 32 ? 5 : (TN <= 64 ? 4 : (TN <= 128 ? 6 : 4))));
   static constexpr int kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5 + 3 * kQ;
@@ -85,15 +105,15 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kAcctOff + 4 * kStages * 4 + 16;
   static constexpr int kMRows = PAIR ? 256 : 128;   // weight rows of one item
   // shared-memory offset of K block j's A / B tile inside a stage
-  __host__ __device__ static constexpr int a_off(int j) { return j * kATileBytes; }
-  __host__ __device__ static constexpr int b_off(int j) { return kKB * kATileBytes + j * kBTileBytes; }
+  __host__ __device__ static constexpr int a_off(int j) { return j * kATile; }
+  __host__ __device__ static constexpr int b_off(int j) { return kKB * kATile + j * kBTileBytes; }
   // LoRA expand chunk j of width lw (16, 32 or 64) packed in a stage: its
   // 128 B rows in the A region, its up-to-kRowsB z rows in the B region
-  // (kKB * 64 / lw chunks per stage; chunk sizes are multiples of the
+  // (kKB * kBK / lw chunks per stage; chunk sizes are multiples of the
   // swizzle atom, so every chunk starts on one)
   __host__ __device__ static constexpr int lora_a_off(int j, int lw) { return j * 128 * lw * 2; }
   __host__ __device__ static constexpr int lora_b_off(int j, int lw) {
-    return kKB * kATileBytes + j * kRowsB * lw * 2;
+    return kKB * kATile + j * kRowsB * lw * 2;
   }
 };
 
@@ -394,9 +414,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             for (int j = 0; j < C::kKB && d * C::kKB + j < nkc; ++j) {
               const int i = d * C::kKB + j;
               const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
-              st_bytes[s] += brows * 128;   // (a stage issued earlier)
-              if (PAIR) tma_load_2d_pair(st + C::b_off(j), tb, fb, kc * 64, brow0);
-              else tma_load_2d(st + C::b_off(j), tb, fb, kc * 64, brow0);
+              st_bytes[s] += brows * C::kBK * 2;   // (a stage issued earlier)
+              if (PAIR) tma_load_2d_pair(st + C::b_off(j), tb, fb, kc * C::kBK, brow0);
+              else tma_load_2d(st + C::b_off(j), tb, fb, kc * C::kBK, brow0);
             }
           }
         }
@@ -433,7 +453,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         const GemmMaps& maps = NPH == 2 && ph ? maps1 : maps0;
         const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
                                     p.shrink);
-        const int nk = (p.K + 63) / 64;             // 64-wide K chunks of the base GEMM
+        const int nk = (p.K + C::kBK - 1) / C::kBK;   // K blocks of the base GEMM
         const bool gate_up = p.mode == kModeGateUp;
         if (p.act_wait) {
           // a down item of the two-phase launch: its token rows are the
@@ -462,7 +482,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
           const int ns0 = min(spc, si.nslot);
           const int ns1 = PAIR ? max(0, si.nslot - spc) : 0;
           const int ns_me = rank == 0 ? ns0 : ns1;
-          const uint32_t per_kb = (ns0 + ns1) * p.r * 128 + (PAIR ? 2 : 1) * brows * 128;
+          const uint32_t per_kb = (ns0 + ns1) * p.r * C::kBK * 2 + (PAIR ? 2 : 1) * brows * C::kBK * 2;
           // a full set of slots on consecutive adapters comes in one box of
           // 128 rows (small per-adapter boxes had made shrink items slow)
           int a_run = -1;
@@ -485,13 +505,14 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             for (int j = 0; j < nkb; ++j) {
               const int kc = kb0 + j;
               if (a_run >= 0) {
-                load4(spc * p.r * 128, st + C::a_off(j), &maps.la_run, fb, kc * 64, 0, ti.expert, a_run);
+                load4(spc * p.r * C::kBK * 2, st + C::a_off(j), &maps.la_run, fb, kc * C::kBK, 0, ti.expert,
+                      a_run);
               } else {
                 for (int q = 0; q < ns_me; ++q)
-                  load4(p.r * 128, st + C::a_off(j) + q * p.r * 128, &maps.la, fb, kc * 64, 0, ti.expert,
-                        p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
+                  load4(p.r * C::kBK * 2, st + C::a_off(j) + q * p.r * C::kBK * 2, &maps.la, fb, kc * C::kBK,
+                        0, ti.expert, p.slot_adapter[si.slot0 + static_cast<int>(rank) * spc + q]);
               }
-              if (waited) load2(brows * 128, st + C::b_off(j), tb, fb, kc * 64, brow0);
+              if (waited) load2(brows * C::kBK * 2, st + C::b_off(j), tb, fb, kc * C::kBK, brow0);
             }
             stage_issued(s);
             if (!waited && ++n_def == C::kStages && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0, brows))
@@ -499,7 +520,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
           }
           if (ok && !waited && !load_deferred_rows(kb_hi - kb_lo, kb_lo, 0, tb, brow0, brows)) ok = false;
         } else {
-          const uint32_t per_kb = (PAIR ? 2 : 1) * (kATileBytes + brows * 128);
+          const uint32_t per_kb = (PAIR ? 2 : 1) * (C::kATile + brows * C::kBK * 2);
           const int kc0 = p.split_k0[it.ks];
           const int nkc = p.split_k0[it.ks + 1] - kc0;
           // (paired tiles, tensor-bound: the token tiles of one expert read
@@ -520,10 +541,10 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
               const int i = i0 + j;
               const int kc = kc0 + (i + rot < nkc ? i + rot : i + rot - nkc);
               if (gate_up)   // 64 features, each gate row followed by its up row, in one box
-                load4(kATileBytes, st + C::a_off(j), &maps.w, fb, kc * 64, 0, grow, ti.expert);
+                load4(C::kATile, st + C::a_off(j), &maps.w, fb, kc * C::kBK, 0, grow, ti.expert);
               else
-                load3(kATileBytes, st + C::a_off(j), &maps.w, fb, kc * 64, grow, ti.expert);
-              if (waited) load2(brows * 128, st + C::b_off(j), tb, fb, kc * 64, brow0);
+                load3(C::kATile, st + C::a_off(j), &maps.w, fb, kc * C::kBK, grow, ti.expert);
+              if (waited) load2(brows * C::kBK * 2, st + C::b_off(j), tb, fb, kc * C::kBK, brow0);
             }
             stage_issued(s);
             if (!waited && ++n_def == C::kStages && !load_deferred_rows(nkc, kc0, rot, tb, brow0, brows))
@@ -548,7 +569,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             // that a LoRA B chunk is read twice in a row (the second from L2)
             const int nl = ti.nslots * p.lora_chunks * p.z_parts;
             const uint32_t per_sub = (PAIR ? 2 : 1) * (128 * lw * 2 + brows * lw * 2);
-            const int cps = C::kKB * 64 / lw;           // chunks packed per stage
+            const int cps = C::kKB * C::kBK / lw;       // chunks packed per stage
             for (int i0 = 0; i0 < nl && ok; i0 += cps, advance()) {
               const int nsub = min(cps, nl - i0);
               const int s = sidx;
@@ -604,7 +625,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         const GemmParams& p = NPH == 2 && ph ? p1 : p0;
         const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
                                     p.shrink);
-        const int nk = (p.K + 63) / 64;
+        const int nk = (p.K + C::kBK - 1) / C::kBK;
         const int nmma = (ti.nrows + 15) & ~15;
         const uint32_t idesc = make_idesc_bf16(nmma, PAIR ? 256 : 128);
         const int buf = li & 1;
@@ -621,7 +642,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
           nb = p.split_k0[it.ks + 1] - p.split_k0[it.ks];
         }
         const int st_base = (nb + C::kKB - 1) / C::kKB;
-        const int cps = p.r > 0 ? C::kKB * 64 / p.lora_w : 1;   // expand chunks per stage
+        const int cps = p.r > 0 ? C::kKB * C::kBK / p.lora_w : 1;   // expand chunks per stage
         const int st_all = st_base + (nl + cps - 1) / cps;
         uint32_t acc = 0;   // the item's first MMA overwrites the accumulator
         // The issuing thread blocks on each MMA (the queue holds about one),
@@ -638,15 +659,15 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             break;
           tc_fence_after();
           const uint32_t st = smem0 + s * C::kStageBytes;
-          if (sti < st_base) {   // base GEMM: K blocks of 64 (4 MMAs of K=16 each)
-            const uint64_t ad0 = make_smem_desc(st + C::a_off(0), 1024u, 2u);
-            const uint64_t bd0 = make_smem_desc(st + C::b_off(0), 1024u, 2u);
+          if (sti < st_base) {   // base GEMM: K blocks of kBK (kBK / 16 MMAs of K=16 each)
+            const uint64_t ad0 = make_smem_desc(st + C::a_off(0), C::kSboK, C::kSwzK);
+            const uint64_t bd0 = make_smem_desc(st + C::b_off(0), C::kSboK, C::kSwzK);
             const int nsub = min(C::kKB, nb - sti * C::kKB);
             if (nsub == C::kKB) {
 #pragma unroll
               for (int j = 0; j < C::kKB; ++j) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < C::kBK / 16; ++kk) {
                   const uint64_t ad = ad0 + static_cast<uint64_t>((C::a_off(j) + kk * 32) >> 4);
                   const uint64_t bd = bd0 + static_cast<uint64_t>((j * C::kBTileBytes + kk * 32) >> 4);
                   if (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, acc); else mma_bf16(d_tmem, ad, bd, idesc, acc);
@@ -656,7 +677,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
             } else {
               for (int j = 0; j < nsub; ++j) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < C::kBK / 16; ++kk) {
                   const uint64_t ad = ad0 + static_cast<uint64_t>((C::a_off(j) + kk * 32) >> 4);
                   const uint64_t bd = bd0 + static_cast<uint64_t>((j * C::kBTileBytes + kk * 32) >> 4);
                   if (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, acc); else mma_bf16(d_tmem, ad, bd, idesc, acc);
@@ -1123,6 +1144,10 @@ size_t moe_gemm_smem_bytes(int tn) {
 }
 
 bool moe_gemm_paired(int tn) { return tn >= 256; }
+
+int moe_gemm_kblock_width(int tn) {
+  return tn >= 256 ? Cfg<256, true>::kBK : Cfg<16, false>::kBK;
+}
 
 int moe_gemm_stage_kblocks(int tn) {
   return tn >= 256 ? Cfg<256, true>::kKB

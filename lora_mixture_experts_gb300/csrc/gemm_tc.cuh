@@ -32,7 +32,8 @@ struct GemmParams {
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
   int group_tiles;     // token tiles per L2 group of the main-item order
   int ksplit;          // K splits of the main items (down mode: fp32 partial per split)
-  // first 64-wide K block of each split, split_k0[ksplit] = K blocks in all;
+  // first K block (moe_gemm_kblock_width wide) of each split,
+  // split_k0[ksplit] = K blocks in all;
   // the last split is the shortest (see split_starts on the host)
   int split_k0[kMaxKSplit + 1];
   long long split_stride;  // elements between the fp32 partials of consecutive splits
@@ -103,7 +104,11 @@ size_t moe_gemm_smem_bytes(int tn);
 // covers 256 weight rows (gate_up: 128 features) instead of 128 (64).
 bool moe_gemm_paired(int tn);
 
-// 64-wide K blocks per pipeline stage for a token-tile width.
+// K blocks per pipeline stage for a token-tile width.
 int moe_gemm_stage_kblocks(int tn);
+
+// Width (elements) of one K block for a token-tile width: the box width of
+// the K-major tensor maps and the unit of GemmParams::split_k0.
+int moe_gemm_kblock_width(int tn);
 
 }  // namespace moelora

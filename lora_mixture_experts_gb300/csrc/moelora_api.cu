@@ -323,8 +323,8 @@ int choose_ksplit(double est_tiles, int n_mtiles, int K, double rows_per_expert)
 // with 3 splits 114.8 -> 112.7 us, T = 8 with 4 splits 93.3 -> 92.8 us; with
 // 2 splits it gained on one workload and lost on another, so those stay
 // uniform).  Uniform splits also when K is too short.
-void set_splits(GemmParams& g, int ksplit, int K) {
-  const int nk = std::max(1, (K + 63) / 64);
+void set_splits(GemmParams& g, int ksplit, int K, int bk) {
+  const int nk = std::max(1, (K + bk - 1) / bk);
   g.ksplit = ksplit;
   const int weight_total = 2 * (ksplit - 1) + 1;
   bool ok = ksplit > 2 && nk >= 2 * weight_total;
@@ -497,10 +497,10 @@ bool enc3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
 // features with each gate row followed by its up row (box row 2i = gate row
 // i, 2i + 1 = up row i), so that the two accumulator rows of a feature land
 // in adjacent TMEM lanes.
-bool enc_gate_up(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint64_t E) {
+bool enc_gate_up(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint64_t E, uint32_t bk) {
   const uint64_t dims[4] = {K, 2, I, E};
   const uint64_t str[3] = {I * K, K, 2 * I * K};
-  const uint32_t box[4] = {64, 2, 64, 1};
+  const uint32_t box[4] = {bk, 2, 64, 1};
   return encode_map(m, base, 4, dims, str, box);
 }
 
@@ -843,23 +843,24 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   // gate_up phase maps
   GemmMaps mg;
   std::memset(&mg, 0, sizeof(mg));
-  bool ok = enc_gate_up(&mg.w, W_gate_up, p.H, p.I, p.E);
-  ok = ok && enc_row_maps(mg.b, x_perm, p.H, p.Pmax, 64, p.tn);
+  const uint32_t bk = static_cast<uint32_t>(moe_gemm_kblock_width(p.tn));
+  bool ok = enc_gate_up(&mg.w, W_gate_up, p.H, p.I, p.E, bk);
+  ok = ok && enc_row_maps(mg.b, x_perm, p.H, p.Pmax, bk, p.tn);
   if (p.lora) {
     ok = ok && enc_gate_up_lora(&mg.lb, B_gu, p.r, p.I, p.E, p.L, lw);
-    ok = ok && enc4(&mg.la, A_gu, p.H, p.r, p.E, p.L, 64, p.r);
-    ok = ok && enc4(&mg.la_run, A_gu, p.H, p.r, p.E, p.L, 64, p.r, 128 / p.r);
+    ok = ok && enc4(&mg.la, A_gu, p.H, p.r, p.E, p.L, bk, p.r);
+    ok = ok && enc4(&mg.la_run, A_gu, p.H, p.r, p.E, p.L, bk, p.r, 128 / p.r);
     ok = ok && enc_row_maps(mg.z, zgu, 2 * p.r, zrows, lw, p.tn);
   }
   // down phase maps
   GemmMaps md;
   std::memset(&md, 0, sizeof(md));
-  ok = ok && enc3(&md.w, W_down, p.I, p.H, p.E, 64, 128);
-  ok = ok && enc_row_maps(md.b, act, p.I, p.Pmax, 64, p.tn);
+  ok = ok && enc3(&md.w, W_down, p.I, p.H, p.E, bk, 128);
+  ok = ok && enc_row_maps(md.b, act, p.I, p.Pmax, bk, p.tn);
   if (p.lora) {
     ok = ok && enc4(&md.lb, B_d, p.r, p.H, p.E, p.L, lw, 128);
-    ok = ok && enc4(&md.la, A_d, p.I, p.r, p.E, p.L, 64, p.r);
-    ok = ok && enc4(&md.la_run, A_d, p.I, p.r, p.E, p.L, 64, p.r, 128 / p.r);
+    ok = ok && enc4(&md.la, A_d, p.I, p.r, p.E, p.L, bk, p.r);
+    ok = ok && enc4(&md.la_run, A_d, p.I, p.r, p.E, p.L, bk, p.r, 128 / p.r);
     ok = ok && enc_row_maps(md.z, zd, p.r, zrows, lw, p.tn);
   }
   if (!ok) return MOELORA_ERR_CUDA;
@@ -867,7 +868,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   GemmParams gu = gemm_params(p, ws, a);
   gu.mode = kModeGateUp;
   gu.K = p.H;
-  set_splits(gu, 1, gu.K);
+  set_splits(gu, 1, gu.K, static_cast<int>(bk));
   const bool paired = moe_gemm_paired(p.tn);
   gu.n_mtiles = (p.I + (paired ? 127 : 63)) / (paired ? 128 : 64);
   gu.out_feats = p.I;
@@ -891,7 +892,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.zbuf = zd;
   gd.out = nullptr;
   gd.out_f32 = ypair;
-  set_splits(gd, p.ksplit, gd.K);
+  set_splits(gd, p.ksplit, gd.K, static_cast<int>(bk));
   gd.split_stride = static_cast<long long>(p.Pmax) * p.H;
   gd.out_ld = p.H;
   gd.work_ctr = &a.hdr->work[1];
@@ -1024,12 +1025,13 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
 
   GemmMaps m;
   std::memset(&m, 0, sizeof(m));
-  bool ok = enc3(&m.w, W, p.H, p.N, 1, 64, 128);
-  ok = ok && enc_row_maps(m.b, x_perm, p.H, p.Pmax, 64, p.tn);
+  const uint32_t bk = static_cast<uint32_t>(moe_gemm_kblock_width(p.tn));
+  bool ok = enc3(&m.w, W, p.H, p.N, 1, bk, 128);
+  ok = ok && enc_row_maps(m.b, x_perm, p.H, p.Pmax, bk, p.tn);
   if (p.lora) {
     ok = ok && enc4(&m.lb, B, p.r, p.N, 1, p.L, lw, 128);
-    ok = ok && enc4(&m.la, A, p.H, p.r, 1, p.L, 64, p.r);
-    ok = ok && enc4(&m.la_run, A, p.H, p.r, 1, p.L, 64, p.r, 128 / p.r);
+    ok = ok && enc4(&m.la, A, p.H, p.r, 1, p.L, bk, p.r);
+    ok = ok && enc4(&m.la_run, A, p.H, p.r, 1, p.L, bk, p.r, 128 / p.r);
     ok = ok && enc_row_maps(m.z, z, p.r, zrows, lw, p.tn);
   }
   if (!ok) return MOELORA_ERR_CUDA;
@@ -1044,7 +1046,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   g.zbuf = z;
   g.out_ld = p.N;
   g.work_ctr = &a.hdr->work[0];
-  set_splits(g, p.ksplit, g.K);
+  set_splits(g, p.ksplit, g.K, static_cast<int>(bk));
   float* partial = p.ksplit > 1 ? ws_ptr<float>(ws, p.off_ypair) : nullptr;
   if (p.ksplit > 1) {
     // fp32 partial per K split (gate weight 1), summed by the combine
