@@ -155,13 +155,13 @@ def workload_name(c):
 
 
 def source_hash():
-    """Hash of the GEMM kernel's sources without their comments and blank
-    space: a DRAM-traffic figure captured by ncu is reported only while the
-    code it measured is unchanged (a comment edit keeps it)."""
+    """Hash of the GEMM and merge kernels' sources without their comments and
+    blank space: a DRAM-traffic figure captured by ncu is reported only while
+    the code it measured is unchanged (a comment edit keeps it)."""
     import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "lora_mixture_experts_gb300", "csrc")
-    for n in ("gemm_tc.cu", "gemm_tc.cuh", "common.cuh"):
+    for n in ("gemm_tc.cu", "gemm_tc.cuh", "common.cuh", "merge.cu", "merge.cuh"):
         with open(os.path.join(d, n)) as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
@@ -684,6 +684,19 @@ def main():
     import torch
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.config.startswith("merge_"):
+        # the merged-weight fast path on its own (one GPU; for profiling)
+        from lora_mixture_experts_gb300 import binding, roofline
+        from lora_mixture_experts_gb300.inputs import CONFIGS
+        binding.load(build_if_missing=True)
+        sampler = ClockSampler(str(device.index))
+        sampler.wait_first()
+        try:
+            res = measure_merge(CONFIGS[args.config[len("merge_"):]], roofline.load_peaks(ROOT), sampler)
+        finally:
+            sampler.stop()
+        print(json.dumps(res), flush=True)
+        return 0
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     try:

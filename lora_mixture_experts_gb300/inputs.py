@@ -89,6 +89,11 @@ for _t in DENSE_T_SWEEP:
 for _t in DENSE_T_SWEEP:
     CONFIGS[f"dense_mlp_t{_t}"] = MoECase(f"dense_mlp_t{_t}", T=_t, H=8192, I=14336, E=1, k=1,
                                           L=32, r=16, adapters="uniform")
+# the skewed layer with a quarter of its experts (4.3 GB of weights instead of
+# 17 GB): a case small enough for multi-pass profiler captures of the same
+# kernel (run with the skewed batch's 256-token tiles)
+CONFIGS["skewed_e16"] = MoECase("skewed_e16", T=256, H=4096, I=11008, E=16, k=6, L=16, r=64,
+                                routing="zipf", adapters="zipf", none_frac=0.1)
 
 
 def bf16_bits(t: torch.Tensor):

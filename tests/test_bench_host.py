@@ -48,7 +48,7 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     not with its comments."""
     d = tmp_path / "lora_mixture_experts_gb300" / "csrc"
     d.mkdir(parents=True)
-    for n in ("gemm_tc.cu", "gemm_tc.cuh", "common.cuh"):
+    for n in ("gemm_tc.cu", "gemm_tc.cuh", "common.cuh", "merge.cu", "merge.cuh"):
         (d / n).write_text("int f() { return 1; }  // one\n/* two */\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.source_hash()
