@@ -35,13 +35,16 @@ struct AlignArgs {
   int* bin_start;               // [nbins]
   WsHeader* hdr;
   // align outputs
-  int* sorted_ids;              // [Pmax]
-  int* blk_expert;              // [Pmax / block_m]
+  int* sorted_ids;              // [Pmax], may be NULL (the forward does not read it)
+  int* blk_expert;              // [Pmax / block_m], may be NULL
   int* seg_off;                 // [nbins + 1], may be NULL
   int* num_post_pad;            // [1], may be NULL
   // forward extras (NULL for the plain align)
   int* row_tok;                 // [Pmax] token of each sorted row, -1 for padding
-  int* row_lora;                // [Pmax] adapter of each row, -2 for padding
+  int* row_lora;                // [Pmax] adapter of each row, -2 for padding; may be NULL
+  // 1: padding rows get row_tok = -1 (and row_lora, row_w) for the permute;
+  // 0 when the rows are gathered by the align itself (nothing reads them)
+  int pad_rows;
   float* row_w;                 // [Pmax] gate weight of each row, 0 for padding
   int* pos_of;                  // [n] sorted row of each entry, -1 if dropped
   // token tiles, LoRA slots and shrink items for the GEMM phases

@@ -147,6 +147,52 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return excl;
 }
 
+// Exclusive scans of three values per thread over the block at once (one
+// pass: two barriers instead of six); warp_sums holds 3 x 32 ints.
+__device__ void block_exclusive_scan3(int v0, int v1, int v2, int* warp_sums, int& e0, int& e1, int& e2,
+                                      int& t0, int& t1, int& t2) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  int x0 = v0, x1 = v1, x2 = v2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y0 = __shfl_up_sync(0xffffffffu, x0, o);
+    const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+    if (lane >= o) {
+      x0 += y0;
+      x1 += y1;
+      x2 += y2;
+    }
+  }
+  if (lane == 31) {
+    warp_sums[warp] = x0;
+    warp_sums[32 + warp] = x1;
+    warp_sums[64 + warp] = x2;
+  }
+  __syncthreads();
+  // the second level: series q by warp q % nwarps (a block may have fewer
+  // than three warps)
+  for (int q = warp; q < 3; q += nwarps) {
+    int v = lane < nwarps ? warp_sums[32 * q + lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sums[32 * q + lane] = v;   // inclusive
+  }
+  __syncthreads();
+  e0 = x0 - v0 + (warp > 0 ? warp_sums[warp - 1] : 0);
+  e1 = x1 - v1 + (warp > 0 ? warp_sums[32 + warp - 1] : 0);
+  e2 = x2 - v2 + (warp > 0 ? warp_sums[64 + warp - 1] : 0);
+  t0 = warp_sums[nwarps - 1];
+  t1 = warp_sums[32 + nwarps - 1];
+  t2 = warp_sums[64 + nwarps - 1];
+  __syncthreads();
+}
+
 // Everything after the per-bin totals: expert counts and padding, segment
 // offsets, padding rows, block experts, and the GEMM tables.  `sb` is a
 // shared-memory array holding the per-bin entry counts; it is turned into
@@ -183,27 +229,37 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
     }
   }
   if (!write) return;
+  // padding and unused rows: the sentinel in sorted_ids (align entry point),
+  // and no token for the permute when it runs (the forward's own tables skip
+  // what nothing reads)
+  const bool pad_tok = a.row_tok != nullptr && a.pad_rows;
   if (has_e) {
-    for (int blk = start / a.block_m; blk < (start + pad) / a.block_m; ++blk) a.blk_expert[blk] = e;
-    for (int p = start + cnt; p < start + pad; ++p) {
-      a.sorted_ids[p] = a.n;
-      if (a.row_tok) {
+    if (a.blk_expert)
+      for (int blk = start / a.block_m; blk < (start + pad) / a.block_m; ++blk) a.blk_expert[blk] = e;
+    if (a.sorted_ids || pad_tok) {
+      for (int p = start + cnt; p < start + pad; ++p) {
+        if (a.sorted_ids) a.sorted_ids[p] = a.n;
+        if (pad_tok) {
+          a.row_tok[p] = -1;
+          if (a.row_lora) a.row_lora[p] = -2;
+          a.row_w[p] = 0.0f;
+        }
+      }
+    }
+  }
+  if (a.sorted_ids || pad_tok) {
+    for (int p = P + tid; p < a.Pmax; p += blockDim.x) {
+      if (a.sorted_ids) a.sorted_ids[p] = a.n;
+      if (pad_tok) {
         a.row_tok[p] = -1;
-        a.row_lora[p] = -2;
+        if (a.row_lora) a.row_lora[p] = -2;
         a.row_w[p] = 0.0f;
       }
     }
   }
-  for (int p = P + tid; p < a.Pmax; p += blockDim.x) {
-    a.sorted_ids[p] = a.n;
-    if (a.row_tok) {
-      a.row_tok[p] = -1;
-      a.row_lora[p] = -2;
-      a.row_w[p] = 0.0f;
-    }
-  }
-  for (int blk = P / a.block_m + tid; blk < a.Pmax / a.block_m; blk += blockDim.x)
-    a.blk_expert[blk] = -1;
+  if (a.blk_expert)
+    for (int blk = P / a.block_m + tid; blk < a.Pmax / a.block_m; blk += blockDim.x)
+      a.blk_expert[blk] = -1;
   if (tid == 0) {
     if (a.seg_off) a.seg_off[a.nbins] = P;
     if (a.num_post_pad) *a.num_post_pad = P;
@@ -232,10 +288,8 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
       }
     }
   }
-  int tot_t, tot_s, tot_h;
-  const int tbase = block_exclusive_scan(n_t, warp_sums, &tot_t);
-  const int sbase = block_exclusive_scan(n_s, warp_sums, &tot_s);
-  const int hbase = block_exclusive_scan(n_h, warp_sums, &tot_h);
+  int tot_t, tot_s, tot_h, tbase, sbase, hbase;
+  block_exclusive_scan3(n_t, n_s, n_h, warp_sums, tbase, sbase, hbase, tot_t, tot_s, tot_h);
   if (has_e && cnt > 0) {
     int sl = sbase, sh = hbase;
     for (int j = 0; j < n_t; ++j) {
@@ -288,7 +342,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
 }
 
 __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
-  __shared__ int warp_sums[32];
+  __shared__ int warp_sums[96];
   extern __shared__ int sb[];   // [nbins]
   grid_dependency_wait();
   grid_dependency_trigger();
@@ -326,7 +380,7 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
 // 1024-thread CTAs the compiler spilled; 48 registers, no spills, measured
 // decode 238.9 -> 238.4 us and dense T = 1 86.7 -> 85.7 us)
 __global__ void __launch_bounds__(kScanThreads, 1) align_small_kernel(AlignArgs a) {
-  __shared__ int warp_sums[32];
+  __shared__ int warp_sums[96];
   extern __shared__ int sm_bins[];   // [nbins] running counts, then [n] positions (gather)
   grid_dependency_wait();
   grid_dependency_trigger();
@@ -384,10 +438,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) align_small_kernel(AlignArgs 
       if (bin < 0 || !MOELORA_IN_RANGE(&a.hdr->err, pos, 0, a.Pmax)) {
         if (a.pos_of) a.pos_of[f] = -1;
       } else {
-        a.sorted_ids[pos] = f;
+        if (a.sorted_ids) a.sorted_ids[pos] = f;
         if (a.row_tok) {
           a.row_tok[pos] = f / a.k;
-          a.row_lora[pos] = bin % (a.L + 1) - 1;
+          if (a.row_lora) a.row_lora[pos] = bin % (a.L + 1) - 1;
           a.row_w[pos] = a.topk_weights ? a.topk_weights[f] : 1.0f;
           a.pos_of[f] = pos;
         }
@@ -429,10 +483,10 @@ __global__ void __launch_bounds__(kAlignChunk) align_scatter_kernel(AlignArgs a)
     if (a.pos_of) a.pos_of[f] = -1;
     return;
   }
-  a.sorted_ids[pos] = f;
+  if (a.sorted_ids) a.sorted_ids[pos] = f;
   if (a.row_tok) {
     a.row_tok[pos] = f / a.k;
-    a.row_lora[pos] = bin % (a.L + 1) - 1;
+    if (a.row_lora) a.row_lora[pos] = bin % (a.L + 1) - 1;
     a.row_w[pos] = a.topk_weights ? a.topk_weights[f] : 1.0f;
     a.pos_of[f] = pos;
   }

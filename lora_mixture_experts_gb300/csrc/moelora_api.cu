@@ -42,8 +42,7 @@ struct Plan {
   int sks = 1;                        // K splits of every shrink item
   int ksplit = 1;                     // K splits of the down / linear phase
   size_t off_hdr = 0, off_chunk_hist = 0, off_bin_of = 0, off_rank_of = 0, off_bin_start = 0;
-  size_t off_sorted = 0, off_blk = 0, off_seg = 0;
-  size_t off_row_tok = 0, off_row_lora = 0, off_row_w = 0, off_pos_of = 0;
+  size_t off_row_tok = 0, off_row_w = 0, off_pos_of = 0;
   size_t off_tiles = 0, off_shrink = 0, off_slot_ad = 0, off_tile_done = 0;
   size_t off_sh_cnt = 0, off_zpart = 0, off_act_done = 0;
   size_t off_xperm = 0, off_zgu = 0, off_zd = 0, off_act = 0, off_ypair = 0;
@@ -272,11 +271,7 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   p.n_slots_max = p.lora ? std::min(p.n, p.E * p.L + p.n_tiles_max) : 0;
   p.n_sh_max = p.n_slots_max;
   p.sks = choose_shrink_splits(p);
-  p.off_sorted = b.take(static_cast<size_t>(p.Pmax) * 4);
-  p.off_blk = b.take(static_cast<size_t>(p.Pmax / p.block_m + 1) * 4);
-  p.off_seg = b.take(static_cast<size_t>(p.nbins + 1) * 4);
   p.off_row_tok = b.take(static_cast<size_t>(p.Pmax) * 4);
-  p.off_row_lora = b.take(static_cast<size_t>(p.Pmax) * 4);
   p.off_row_w = b.take(static_cast<size_t>(p.Pmax) * 4);
   p.off_pos_of = b.take(static_cast<size_t>(p.n) * 4);
   p.off_tiles = b.take(static_cast<size_t>(p.n_tiles_max) * sizeof(TileInfo));
@@ -587,6 +582,8 @@ cudaError_t run_align(Launcher& ln, AlignArgs a, cudaStream_t stream, int num_sm
   }
   if (a.n > 0 && align_small_fits(a)) {
     a.reset_err = 1;
+    // rows gathered here: no permute reads the padding rows' tokens
+    if (a.x && !a.logits) a.pad_rows = 0;
     ln.before("align_small");
     if ((e = launch_align_small(a, stream, true, num_sms)) != cudaSuccess) return e;
     if (gathered) *gathered = a.x != nullptr && a.logits == nullptr;
@@ -653,12 +650,16 @@ AlignArgs align_args(const Plan& p, void* ws) {
 }
 
 void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
-  a.sorted_ids = ws_ptr<int>(ws, p.off_sorted);
-  a.blk_expert = ws_ptr<int>(ws, p.off_blk);
-  a.seg_off = ws_ptr<int>(ws, p.off_seg);
+  // the forward reads the rows' tokens, weights and positions and the GEMM
+  // tables; the sorted order, block experts, segment offsets and row
+  // adapters of the align entry point are not written
+  a.sorted_ids = nullptr;
+  a.blk_expert = nullptr;
+  a.seg_off = nullptr;
   a.num_post_pad = nullptr;
   a.row_tok = ws_ptr<int>(ws, p.off_row_tok);
-  a.row_lora = ws_ptr<int>(ws, p.off_row_lora);
+  a.row_lora = nullptr;
+  a.pad_rows = 1;
   a.row_w = ws_ptr<float>(ws, p.off_row_w);
   a.pos_of = ws_ptr<int>(ws, p.off_pos_of);
   a.tn = p.tn;
