@@ -274,8 +274,11 @@ int moe_lora_merge_adapter(const moelora_dims* d, int32_t adapter,
  * `path` is a file or a folder (every *.cfg file in it, in name order); NULL
  * clears the table.  Each line: `moe` or `linear`, then key=value tokens;
  * shape keys T (value or range lo-hi), k, E, H, I (linear: K, N), L, r must
- * match when present; choice keys tn (token tile 16/32/64/128/256) and
- * ksplit (1..4, K splits of the down / linear phase) override the built-in
+ * match when present; choice keys tn (token tile 16/32/64/128/256),
+ * ksplit (1..4, K splits of the down / linear phase), phases (1: one launch
+ * per projection, 2: both in one launch, single-CTA tiles) and guksplit
+ * (1..4, K splits of the gate_up phase on single-CTA tiles, whose fp32 parts
+ * the last split to arrive sums in split order) override the built-in
  * choice; the first matching line wins; '#' starts a comment.  Workspace
  * sizes depend on the choice: load the table before sizing workspaces.
  * Returns MOELORA_ERR_INVALID_ARG for a missing path or a malformed line

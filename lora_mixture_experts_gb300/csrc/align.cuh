@@ -57,6 +57,8 @@ struct AlignArgs {
   int* slot_adapter;
   int* tile_done;
   int* act_done;                // [tiles] gate_up items done per tile (two-phase launch), or NULL
+  int* gu_cnt;                  // [tiles * gu_nm] split arrivals of the K-split gate_up, or NULL
+  int gu_nm;
   // 1: the single-CTA align zeroes the workspace error word before anything
   // can flag it (the call then needs no separate memset)
   int reset_err;

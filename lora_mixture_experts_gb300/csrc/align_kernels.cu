@@ -290,6 +290,8 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
   }
   int tot_t, tot_s, tot_h, tbase, sbase, hbase;
   block_exclusive_scan3(n_t, n_s, n_h, warp_sums, tbase, sbase, hbase, tot_t, tot_s, tot_h);
+  if (a.gu_cnt)   // the K-split gate_up's arrival counters, one per (tile, weight tile)
+    for (int i = tid; i < tot_t * a.gu_nm; i += blockDim.x) a.gu_cnt[i] = 0;
   if (has_e && cnt > 0) {
     int sl = sbase, sh = hbase;
     for (int j = 0; j < n_t; ++j) {

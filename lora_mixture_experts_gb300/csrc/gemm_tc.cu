@@ -932,18 +932,82 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
               orow[static_cast<size_t>(c) * p.out_ld] = __float2bfloat16_rn(silu_f(g) * u);
           }
         };
-        int c0 = 0;
-        for (; c0 + 32 <= nmma; c0 += 32) {
-          float v[32];
-          tmem_ld32(t_row + c0, v);
-          finish(v, c0, 16);
+        bool last = true;
+        if (p.ksplit > 1) {
+          // K split: this split's fp32 part of every column, then its
+          // arrival; the split that arrives last (whichever it is) sums the
+          // parts in split order, so the result does not depend on timing
+          const size_t slot = static_cast<size_t>(it.tile) * p.n_mtiles + it.m;
+          auto part_of = [&](int s) {
+            return p.gu_part + ((static_cast<size_t>(s) * p.gu_slots + slot) * 128 + row) * TN;
+          };
+          float* mine_part = part_of(it.ks);
+          for (int c0 = 0; c0 < nmma; c0 += 16) {
+            float v[16];
+            tmem_ld16(t_row + c0, v);
+#pragma unroll
+            for (int cc = 0; cc < 16; cc += 4)
+              *reinterpret_cast<float4*>(mine_part + c0 + cc) = make_float4(v[cc], v[cc + 1], v[cc + 2], v[cc + 3]);
+          }
+          named_bar_sync(1, 128);
+          bool mine = false;
+          if (row == 0) {
+            __threadfence();
+            mine = atomicAdd(&p.gu_cnt[slot], 1) + 1 == p.ksplit;
+            __threadfence();
+          }
+          last = bar_red_or(1, 128, mine);
+          if (last) {
+            int c0 = 0;
+            for (; c0 + 32 <= nmma; c0 += 32) {
+              float v[32];
+#pragma unroll
+              for (int cc = 0; cc < 32; ++cc) v[cc] = 0.0f;
+              for (int s = 0; s < p.ksplit; ++s) {
+                const float4* ps = reinterpret_cast<const float4*>(part_of(s) + c0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 w = __ldcg(ps + q);
+                  v[4 * q] += w.x;
+                  v[4 * q + 1] += w.y;
+                  v[4 * q + 2] += w.z;
+                  v[4 * q + 3] += w.w;
+                }
+              }
+              finish(v, c0, 16);
+            }
+            if (c0 < nmma) {   // a last chunk of 16 columns
+              float v[16];
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) v[cc] = 0.0f;
+              for (int s = 0; s < p.ksplit; ++s) {
+                const float4* ps = reinterpret_cast<const float4*>(part_of(s) + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float4 w = __ldcg(ps + q);
+                  v[4 * q] += w.x;
+                  v[4 * q + 1] += w.y;
+                  v[4 * q + 2] += w.z;
+                  v[4 * q + 3] += w.w;
+                }
+              }
+              finish(v, c0, 8);
+            }
+          }
+        } else {
+          int c0 = 0;
+          for (; c0 + 32 <= nmma; c0 += 32) {
+            float v[32];
+            tmem_ld32(t_row + c0, v);
+            finish(v, c0, 16);
+          }
+          if (c0 < nmma) {   // a last chunk of 16 columns
+            float v[16];
+            tmem_ld16(t_row + c0, v);
+            finish(v, c0, 8);
+          }
         }
-        if (c0 < nmma) {   // a last chunk of 16 columns
-          float v[16];
-          tmem_ld16(t_row + c0, v);
-          finish(v, c0, 8);
-        }
-        if (p.act_count) {
+        if (last && p.act_count) {
           // two-phase launch: publish this item's activation rows to the
           // tile's down items (every thread's stores, then one release)
           named_bar_sync(1, 128);

@@ -31,7 +31,8 @@ struct GemmParams {
   int lora_swz;        // descriptor layout code of a LoRA chunk
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
   int group_tiles;     // token tiles per L2 group of the main-item order
-  int ksplit;          // K splits of the main items (down mode: fp32 partial per split)
+  int ksplit;          // K splits of the main items (down mode: fp32 partial per split;
+                       // gate_up: parts summed by the last split, see gu_part)
   // first K block (moe_gemm_kblock_width wide) of each split,
   // split_k0[ksplit] = K blocks in all;
   // the last split is the shortest (see split_starts on the host)
@@ -78,6 +79,14 @@ struct GemmParams {
   __nv_bfloat16* out;   // act [Pmax][I] (gate_up) or out [T][N] (linear)
   float* out_f32;       // y_pair [Pmax][H] (down): gate-weighted expert output, fp32
   int out_ld;
+  // gate_up split over K (ksplit > 1, single-CTA tiles): each split writes
+  // its fp32 part of the item's 128 accumulator rows to gu_part
+  // [ksplit][gu_slots][128][tn] (slot = tile * n_mtiles + m) and counts on
+  // gu_cnt[slot] (zeroed by the align); the split that arrives last sums the
+  // parts in split order and applies SiLU(gate) * up
+  float* gu_part;
+  int* gu_cnt;
+  int gu_slots;
   int* work_ctr;        // items claimed so far (zeroed by the align); NULL = fixed shares
   int early_weights;    // 1: on unpaired tiles, stream the first weight blocks before
                         //    the preceding launch has finished (see the kernel)

@@ -41,12 +41,14 @@ struct Plan {
   int n_tiles_max = 0, n_slots_max = 0, n_sh_max = 0;
   int sks = 1;                        // K splits of every shrink item
   int ksplit = 1;                     // K splits of the down / linear phase
+  int gksplit = 1;                    // K splits of the gate_up phase (single-CTA tiles)
   size_t off_hdr = 0, off_chunk_hist = 0, off_bin_of = 0, off_rank_of = 0, off_bin_start = 0;
   size_t off_row_tok = 0, off_row_w = 0, off_pos_of = 0;
   size_t off_tiles = 0, off_shrink = 0, off_slot_ad = 0, off_tile_done = 0;
   size_t off_sh_cnt = 0, off_zpart = 0, off_act_done = 0;
   size_t off_xperm = 0, off_zgu = 0, off_zd = 0, off_act = 0, off_ypair = 0;
   size_t off_topk_ids = 0, off_topk_w = 0;   // router results (routed forward)
+  size_t off_gupart = 0, off_gucnt = 0;      // K-split gate_up parts and arrival counters
   size_t total = 0;
 };
 
@@ -92,7 +94,7 @@ struct TuneEntry {
   bool linear = false;
   int t_lo = 0, t_hi = 0x7fffffff;
   int k = -1, E = -1, H = -1, I = -1, L = -1, r = -1;   // H = K, I = N for linear
-  int tn = 0, ksplit = 0, phases = 0;
+  int tn = 0, ksplit = 0, phases = 0, guksplit = 0;
 };
 
 std::mutex g_tune_mu;
@@ -145,6 +147,9 @@ bool parse_tune_line(const std::string& line, TuneEntry& e, bool& is_entry) {
     } else if (key == "phases") {
       if (iv < 1 || iv > 2) return false;
       e.phases = iv;
+    } else if (key == "guksplit") {
+      if (iv < 1 || iv > 4) return false;
+      e.guksplit = iv;
     } else {
       return false;
     }
@@ -167,7 +172,7 @@ int load_tune_file(const std::string& path, std::vector<TuneEntry>& out) {
 
 // Choice for a shape from the loaded table (tn, ksplit; 0 = no override).
 void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, int& tn, int& ks,
-                 int* phases = nullptr) {
+                 int* phases = nullptr, int* guksplit = nullptr) {
   std::lock_guard<std::mutex> lk(g_tune_mu);
   for (const TuneEntry& e : g_tune) {
     if (e.linear != linear || T < e.t_lo || T > e.t_hi) continue;
@@ -177,6 +182,7 @@ void tune_lookup(bool linear, int T, int k, int E, int H, int I, int L, int r, i
     if (e.tn) tn = e.tn;
     if (e.ksplit) ks = e.ksplit;
     if (phases && e.phases) *phases = e.phases;
+    if (guksplit && e.guksplit) *guksplit = e.guksplit;
     return;
   }
 }
@@ -310,6 +316,24 @@ int choose_ksplit(double est_tiles, int n_mtiles, int K, double rows_per_expert)
   return eff(2 * items) >= eff(items) ? 2 : 1;
 }
 
+// K splits of the gate_up phase.  Its items cannot be split like the down
+// phase's (the activation needs the whole sum), so a split writes its fp32
+// part and the last split to arrive sums the parts and applies SiLU * up.
+// Meant for layers whose gate_up phase has few items for the persistent
+// grid (one expert: I / 64 weight tiles, 224 for I = 14336, 1.47 waves of
+// 152 SMs).  Measured on the dense MLP (same box): T = 1 129.6 -> 127.4 us
+// with 2 splits and two launches, T = 8 139.3 -> 137.3 us with 2 splits in
+// the two-phase launch, T = 64 188.6 -> 200.0 us (worse: the summing split's
+// epilogue holds its accumulator).  So the built-in choice is no split; the
+// tuning table's `guksplit` key (or MOELORA_GU_KSPLIT) sets it per workload.
+// Single-CTA tiles only, at least 16 K blocks per split.
+int choose_gate_up_ksplit(int K, bool paired) {
+  if (paired) return 1;
+  const int nk = (K + 63) / 64;
+  const int s = env_override("MOELORA_GU_KSPLIT", 1, 4);
+  return std::max(1, std::min({s > 0 ? s : 1, 4, nk / 16}));
+}
+
 // K-block starts of the splits of a GEMM phase.  The main items are claimed
 // split by split, so the last split's items are the ones a finishing SM
 // takes last; from three splits up that split gets half the K blocks of the
@@ -374,6 +398,18 @@ Plan plan_forward(const moelora_dims* d) {
   }
   p.ksplit = clamp_ksplit(p.ksplit, p.I);
   p.off_ypair = b.take(static_cast<size_t>(p.ksplit) * p.Pmax * p.H * 4);
+  p.gksplit = choose_gate_up_ksplit(p.H, moe_gemm_paired(p.tn));
+  {
+    int t_tn = 0, t_ks = 0, t_gks = 0;
+    tune_lookup(false, p.T, p.k, p.E, p.H, p.I, p.L, p.r, t_tn, t_ks, nullptr, &t_gks);
+    if (t_gks && !env_override("MOELORA_GU_KSPLIT", 1, 4) && !moe_gemm_paired(p.tn))
+      p.gksplit = std::max(1, std::min(t_gks, ((p.H + 63) / 64) / 16));
+  }
+  if (p.gksplit > 1) {
+    const size_t slots = static_cast<size_t>(p.n_tiles_max) * ((p.I + 63) / 64);
+    p.off_gupart = b.take(static_cast<size_t>(p.gksplit) * slots * 128 * p.tn * 4);
+    p.off_gucnt = b.take(slots * 4);
+  }
   p.total = b.cur;
   return p;
 }
@@ -683,6 +719,8 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
   a.sh_cnt = ws_ptr<int>(ws, p.off_sh_cnt);
   a.slot_adapter = ws_ptr<int>(ws, p.off_slot_ad);
   a.tile_done = ws_ptr<int>(ws, p.off_tile_done);
+  a.gu_cnt = p.gksplit > 1 ? ws_ptr<int>(ws, p.off_gucnt) : nullptr;
+  a.gu_nm = p.gksplit > 1 ? (p.I + 63) / 64 : 0;
 }
 
 GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
@@ -869,7 +907,12 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   GemmParams gu = gemm_params(p, ws, a);
   gu.mode = kModeGateUp;
   gu.K = p.H;
-  set_splits(gu, 1, gu.K, static_cast<int>(bk));
+  set_splits(gu, p.gksplit, gu.K, static_cast<int>(bk));
+  if (p.gksplit > 1) {
+    gu.gu_part = ws_ptr<float>(ws, p.off_gupart);
+    gu.gu_cnt = a.gu_cnt;
+    gu.gu_slots = p.n_tiles_max * ((p.I + 63) / 64);
+  }
   const bool paired = moe_gemm_paired(p.tn);
   gu.n_mtiles = (p.I + (paired ? 127 : 63)) / (paired ? 128 : 64);
   gu.out_feats = p.I;
@@ -921,7 +964,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
     a.act_done = act_done;          // zeroed by the align
     gu.act_count = act_done;
     gd.act_wait = act_done;
-    gd.act_target = gu.n_mtiles * gu.ksplit;
+    gd.act_target = gu.n_mtiles;   // one count per weight tile (the last K split's)
   }
 
   Launcher ln(stream);
@@ -940,10 +983,11 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   if (two_phase) {
     ln.before("gemm_gate_up_down");
     MOELORA_CUDA_CHECK(launch_moe_gemm_two_phase(
-        p.tn, mg, gu, md, gd, gemm_grid(p, gu.n_mtiles + gd.n_mtiles * p.ksplit, sms), stream));
+        p.tn, mg, gu, md, gd, gemm_grid(p, gu.n_mtiles * p.gksplit + gd.n_mtiles * p.ksplit, sms),
+        stream));
   } else {
     ln.before("gemm_gate_up");
-    MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles, sms), stream));
+    MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, mg, gu, gemm_grid(p, gu.n_mtiles * p.gksplit, sms), stream));
     ln.before("gemm_down");
     MOELORA_CUDA_CHECK(launch_moe_gemm(p.tn, md, gd, gemm_grid(p, gd.n_mtiles * p.ksplit, sms), stream));
   }

@@ -5,9 +5,10 @@ tuning tables for ``moelora_load_tuning``.
 
 A family is one layer shape (k, E, H, I, L, r, or K, N, L, r for the dense
 linear) swept over a ladder of batch sizes T.  At every T of the ladder each
-candidate (token tile tn, K split, and on single-CTA tiles one or two
-launches for the projections) is forced with a one-line table and the whole
-layer call is timed with CUDA events.  The ladder then becomes batch-size
+candidate (token tile tn, K split, on single-CTA tiles one or two launches
+for the projections, and on a one-expert layer a K split of the gate_up
+phase) is forced with a one-line table and the whole layer call is timed
+with CUDA events.  The ladder then becomes batch-size
 buckets: the bucket of a sampled T reaches halfway (geometrically) to its
 neighbours, the last one to any larger T, and neighbouring buckets with the
 same winner merge into one `T=lo-hi` line.  A bucket whose winner is within
@@ -150,11 +151,14 @@ def best_choice(case, device, cand_file, log=print):
     for tn in TILES:
         if tn > 16 and tn // 2 >= max(case.T * getattr(case, "k", 1), 16):
             continue     # a tile more than twice the whole batch only adds padding
-        # both projections in one launch is an option on single-CTA tiles
+        # both projections in one launch is an option on single-CTA tiles,
+        # and on a one-expert layer a K-split gate_up phase
         phase_opts = (1, 2) if (not isinstance(case, LinearCase) and tn < 256) else (0,)
-        for ks in ((1,) if tn == 256 else (1, 2, 3, 4)):
-            for ph in phase_opts:
-                choice = f"tn={tn} ksplit={ks}" + (f" phases={ph}" if ph else "")
+        gu_opts = (1, 2, 3) if (not isinstance(case, LinearCase) and tn < 256 and case.E == 1) else (1,)
+        for ks, ph, gks in [(ks, ph, g) for ks in ((1,) if tn == 256 else (1, 2, 3, 4))
+                            for ph in phase_opts for g in gu_opts]:
+                choice = (f"tn={tn} ksplit={ks}" + (f" phases={ph}" if ph else "") +
+                          (f" guksplit={gks}" if gks > 1 else ""))
                 with open(cand_file, "w") as f:
                     f.write(f"{line0} {choice}\n")
                 binding.moelora_load_tuning(cand_file)

@@ -256,6 +256,31 @@ def test_forward_shrink_split_k(monkeypatch, shape, splits):
     assert torch.equal(out, again)          # the order of arrival does not matter
 
 
+# H >= 48 K blocks so that three splits keep at least 16 K blocks each
+GU_SPLIT_SHAPES = [(8, 3072, 2048, 1, 1, 4, 16), (40, 3072, 1024, 3, 2, 3, 32), (70, 3200, 520, 2, 2, 2, 64)]
+
+
+@pytest.mark.parametrize("two_phase", ["0", "1"])
+@pytest.mark.parametrize("splits", [2, 3])
+@pytest.mark.parametrize("shape", GU_SPLIT_SHAPES,
+                         ids=[f"T{s[0]}_H{s[1]}_I{s[2]}_E{s[3]}_k{s[4]}_L{s[5]}_r{s[6]}" for s in GU_SPLIT_SHAPES])
+def test_forward_gate_up_split_k(monkeypatch, shape, splits, two_phase):
+    """The gate_up phase cut into K splits (forced): each split's fp32 part
+    is summed in split order by the last split to arrive, which applies
+    SiLU(gate) * up; with one launch per projection and with both in one
+    launch (whose down items then wait for one count per weight tile)."""
+    T, H, I, E, k, L, r = shape
+    d = make_moe_case(small_moe_case(T, H, I, E, k, L, r), seed=31, device=DEV)
+    dims = binding.dims_of(d["x"], d["topk_ids"], d["W_gate_up"], d["W_down"], d["A_gu"])
+    unsplit = binding.moelora_workspace_bytes(dims)
+    monkeypatch.setenv("MOELORA_GU_KSPLIT", str(splits))
+    monkeypatch.setenv("MOELORA_TWO_PHASE", two_phase)
+    assert binding.moelora_workspace_bytes(dims) > unsplit   # the split's parts are planned
+    out = _run_parity(d, what=f"{shape} gate_up splits {splits}")
+    again = _gpu_forward(d)
+    assert torch.equal(out, again)          # the order of arrival does not matter
+
+
 @pytest.mark.parametrize("shape", _random_shapes(24, 17), ids=lambda s: "T{T}_H{H}_I{I}_E{E}_k{k}_L{L}_r{r}".format(**s))
 def test_forward_random_shapes(shape):
     s = shape
