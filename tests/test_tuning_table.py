@@ -113,3 +113,19 @@ def test_sweep_lines_merge_buckets_and_load(tmp_path):
     base = binding.moelora_workspace_bytes(moelora_dims(8, 4, 32, 2880, 2880, 8, 32))
     binding.moelora_load_tuning(None)
     assert binding.moelora_workspace_bytes(moelora_dims(8, 4, 32, 2880, 2880, 8, 32)) != base
+
+
+def test_gate_up_split_key(tmp_path):
+    # a one-expert layer: guksplit plans the gate_up phase's fp32 parts
+    # (visible as a larger workspace); out-of-range values are rejected
+    mlp = moelora_dims(8, 1, 1, 8192, 14336, 32, 16)
+    base = binding.moelora_workspace_bytes(mlp)
+    binding.moelora_load_tuning(_write(tmp_path, "g.cfg", "moe T=1-22 E=1 tn=16 guksplit=2\n"))
+    assert binding.moelora_workspace_bytes(mlp) > base
+    with pytest.raises(MoeLoraError):
+        binding.moelora_load_tuning(_write(tmp_path, "bad.cfg", "moe T=8 guksplit=5\n"))
+    # CTA-pair tiles keep one gate_up split
+    binding.moelora_load_tuning(_write(tmp_path, "p.cfg", "moe T=1-22 E=1 tn=256 guksplit=2\n"))
+    w256 = binding.moelora_workspace_bytes(mlp)
+    binding.moelora_load_tuning(_write(tmp_path, "q.cfg", "moe T=1-22 E=1 tn=256\n"))
+    assert binding.moelora_workspace_bytes(mlp) == w256
