@@ -51,6 +51,7 @@ struct AlignArgs {
   int tn;                       // token tile width
   int spi;                      // slots per shrink item (128 / r); 0 = no LoRA
   int sks;                      // K splits of every shrink item (>= 1)
+  int grp_max;                  // tiles per L2 group of the main-item order (1..255)
   TileInfo* tiles;
   ShrinkItem* shrink;           // [shrink items * sks], the splits of an item adjacent
   int* sh_cnt;                  // [2 * shrink items] split arrivals per item and CTA of a pair

@@ -292,6 +292,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
   block_exclusive_scan3(n_t, n_s, n_h, warp_sums, tbase, sbase, hbase, tot_t, tot_s, tot_h);
   if (a.gu_cnt)   // the K-split gate_up's arrival counters, one per (tile, weight tile)
     for (int i = tid; i < tot_t * a.gu_nm; i += blockDim.x) a.gu_cnt[i] = 0;
+  const int gmax = min(255, max(1, a.grp_max));
   if (has_e && cnt > 0) {
     int sl = sbase, sh = hbase;
     for (int j = 0; j < n_t; ++j) {
@@ -303,7 +304,11 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
       ti.nrows = s1 - s0;
       ti.slot_base = sl;
       ti.sh_base = sh * a.sks;
-      ti.pad_ = 0;
+      {
+        // the expert's tiles in runs of at most gmax (the last run takes the rest)
+        const int g0 = j / gmax * gmax;
+        ti.grp = ((tbase + g0) << 8) | min(gmax, n_t - g0);
+      }
       int ns = 0;
       if (a.spi > 0) {
         for (int l = 1; l < Lp; ++l) {

@@ -21,7 +21,10 @@ struct TileInfo {
   int nslots;     // adapters >= 0 present in the tile, one slot each
   int sh_base;    // first shrink item of the tile
   int nsh;        // shrink items of the tile
-  int pad_;
+  // L2 group of the main-item order that holds this tile: first tile * 256 +
+  // tiles in the group (1..255).  A group is a run of consecutive tiles of
+  // one expert, at most the align's group cap long.
+  int grp;
 };
 
 // One shrink item: the LoRA shrink of up to 128/r slots of one tile, over

@@ -131,12 +131,23 @@ struct Item {
 };
 
 // Item order: all shrink items first, then the main items, K split by K
-// split; inside a split, groups of `gt` consecutive token tiles.  Inside a
-// group the weight tile m is the slow index and the tile the fast one, so the
-// tiles of one expert (adjacent in the tile table) share each weight tile
-// through L2 while it is hot, and the group's token rows (sized by the host
-// to a fraction of L2) stay resident across all m.
-__device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_m, int gt,
+// split; inside a split, the token tiles' L2 groups in tile order.  A group is
+// a run of consecutive tiles of one expert (written by the align into each
+// tile's `grp`); inside it the weight tile m is the slow index and the tile
+// the fast one, so the tiles of an expert read each weight tile one after
+// the other while it is hot in L2, and the group's token rows (the align caps
+// the run length) stay resident across all m.  A group of tiles [g0, g0+gn)
+// holds the split's items [g0 * n_m, (g0 + gn) * n_m), so the group of a main
+// item is the group of tile w / n_m (its anchor).
+__device__ __forceinline__ int main_item_anchor(int w, int n_sh, int n_tiles, int n_m) {
+  w -= n_sh;
+  const int per_split = n_tiles * n_m;
+  return (w % per_split) / n_m;
+}
+
+// `grp`: the group of the item's tile (any tile of the group; ignored for
+// shrink items).
+__device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_m, int grp,
                                             const ShrinkItem* sh) {
   Item it;
   if (w < n_sh) {
@@ -150,15 +161,13 @@ __device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_
     const int per_split = n_tiles * n_m;
     it.ks = w / per_split;
     w -= it.ks * per_split;
-    const int per_group = gt * n_m;
-    const int g = w / per_group;
-    const int wl = w - g * per_group;
-    const int t0 = g * gt;
-    const int ntg = min(gt, n_tiles - t0);
+    const int g0 = grp >> 8;
+    const int gn = max(1, grp & 255);
+    const int wl = w - g0 * n_m;
     it.shrink = 0;
     it.sh = -1;
-    it.m = wl / ntg;
-    it.tile = t0 + (wl - it.m * ntg);
+    it.m = wl / gn;
+    it.tile = g0 + (wl - it.m * gn);
   }
   return it;
 }
@@ -451,7 +460,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         const int ph = NPH == 2 && w >= items0 ? 1 : 0;
         const GemmParams& p = NPH == 2 && ph ? p1 : p0;
         const GemmMaps& maps = NPH == 2 && ph ? maps1 : maps0;
-        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
+        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, ti.grp,
                                     p.shrink);
         const int nk = (p.K + C::kBK - 1) / C::kBK;   // K blocks of the base GEMM
         const bool gate_up = p.mode == kModeGateUp;
@@ -623,7 +632,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         if (w < 0) break;
         const int ph = NPH == 2 && w >= items0 ? 1 : 0;
         const GemmParams& p = NPH == 2 && ph ? p1 : p0;
-        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
+        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, ti.grp,
                                     p.shrink);
         const int nk = (p.K + C::kBK - 1) / C::kBK;
         const int nmma = (ti.nrows + 15) & ~15;
@@ -759,8 +768,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         if (w >= 0) {
           const bool w1 = NPH == 2 && w >= items0;
           const GemmParams& pw = w1 ? p1 : p0;
-          ti = p.tiles[decode_item(w - (w1 ? items0 : 0), n_sh, n_tiles, pw.n_mtiles, pw.group_tiles,
-                                   p.shrink).tile];
+          const int wl = w - (w1 ? items0 : 0);
+          const int grp = wl < n_sh ? 0 : p.tiles[main_item_anchor(wl, n_sh, n_tiles, pw.n_mtiles)].grp;
+          ti = p.tiles[decode_item(wl, n_sh, n_tiles, pw.n_mtiles, grp, p.shrink).tile];
         }
         ring[q].ti = ti;
         ring[q].w = w;
@@ -806,7 +816,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
       if (w < 0) break;
       const int ph = NPH == 2 && w >= items0 ? 1 : 0;
       const GemmParams& p = NPH == 2 && ph ? p1 : p0;
-      const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, p.group_tiles,
+      const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, ti.grp,
                                   p.shrink);
       const bool gate_up = p.mode == kModeGateUp;
       const int nmma = (ti.nrows + 15) & ~15;

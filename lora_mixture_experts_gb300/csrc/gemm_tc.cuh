@@ -30,7 +30,6 @@ struct GemmParams {
   int lora_chunks;     // r / lora_w
   int lora_swz;        // descriptor layout code of a LoRA chunk
   int done_target;     // shrink items a tile must see done: 1x or 2x its nsh
-  int group_tiles;     // token tiles per L2 group of the main-item order
   int ksplit;          // K splits of the main items (down mode: fp32 partial per split;
                        // gate_up: parts summed by the last split, see gu_part)
   // first K block (moe_gemm_kblock_width wide) of each split,

@@ -648,20 +648,14 @@ cudaError_t run_align(Launcher& ln, AlignArgs a, cudaStream_t stream, int num_sm
   return cudaSuccess;
 }
 
-// Token tiles per group of the main-item order (inside a group the weight
-// tile m is the slow index and the token tile the fast one).  One tile per
-// group makes the concurrent items of the persistent grid all weight tiles of
-// one to a few consecutive token tiles, so an expert's tiles read each weight
-// tile together while the grid has room for all of them; when one tile's
-// weight tiles alone fill the grid, a group holds the expert's expected tiles
-// so that they still do.  Measured on GB300 against groups sized to 32 MB of
-// L2: 3.5% faster on the prefill batch, 2.3% on the skewed batch, the same on
-// the decode batch; the dense T=512 linear (two tiles of one weight) needs
-// its two tiles in one group or it reads the weights twice.
-int group_tiles(int tn, int n_m, double rows_per_expert, int units) {
-  if (const int f = env_override("MOELORA_GROUP_TILES", 1, 1 << 20)) return f;
-  const int tpe = std::max(1, static_cast<int>(std::ceil(rows_per_expert / tn)));
-  return static_cast<long long>(n_m) * tpe > units ? tpe : 1;
+// Token tiles per L2 group of the main-item order (at most; a group is a run
+// of one expert's tiles, and inside it the weight tile m is the slow index).
+// The tiles of an expert then read each weight tile one after the other, and
+// the run's token rows, at most ~16 MB of them, stay in L2 across all m.
+int group_cap(int tn, int kmax) {
+  if (const int f = env_override("MOELORA_GROUP_TILES", 1, 255)) return f;
+  const double tile_bytes = static_cast<double>(tn) * kmax * 2.0;
+  return static_cast<int>(std::max(1.0, std::min(255.0, std::floor(16.0 * (1 << 20) / tile_bytes))));
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
@@ -714,6 +708,7 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
                            : (p.sks > 1 ? 128 / p.r : std::max(1, 128 / (p.r * p.ksplit))))
                  : 0;
   a.sks = p.sks;
+  a.grp_max = group_cap(p.tn, std::max(p.H, p.I));
   a.tiles = ws_ptr<TileInfo>(ws, p.off_tiles);
   a.shrink = ws_ptr<ShrinkItem>(ws, p.off_shrink);
   a.sh_cnt = ws_ptr<int>(ws, p.off_sh_cnt);
@@ -917,9 +912,6 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gu.n_mtiles = (p.I + (paired ? 127 : 63)) / (paired ? 128 : 64);
   gu.out_feats = p.I;
   gu.done_target = first_phase_done_target();
-  const int units = paired ? sms / 2 : sms;
-  const double rows_per_expert = static_cast<double>(p.n) / p.E;
-  gu.group_tiles = group_tiles(p.tn, gu.n_mtiles, rows_per_expert, units);
   gu.zbuf = zgu;
   gu.z_parts = 2;   // the gate_up shrink result as a bf16 hi/lo pair
   gu.out = act;
@@ -932,7 +924,6 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   gd.n_mtiles = (p.H + (paired ? 255 : 127)) / (paired ? 256 : 128);
   gd.out_feats = p.H;
   gd.done_target = 2;
-  gd.group_tiles = group_tiles(p.tn, gd.n_mtiles, rows_per_expert, units);
   gd.zbuf = zd;
   gd.out = nullptr;
   gd.out_f32 = ypair;
@@ -1087,7 +1078,6 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   g.n_mtiles = (p.N + (paired ? 255 : 127)) / (paired ? 256 : 128);
   g.out_feats = p.N;
   g.done_target = first_phase_done_target();
-  g.group_tiles = group_tiles(p.tn, g.n_mtiles, static_cast<double>(p.T), paired ? sms / 2 : sms);
   g.zbuf = z;
   g.out_ld = p.N;
   g.work_ctr = &a.hdr->work[0];
