@@ -269,8 +269,10 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
 
   // token tiles of tn rows per expert; one LoRA slot per adapter (>= 0)
   // present in a tile; shrink items of up to spi slots
+  __shared__ int s_nh_max;   // most shrink items of any one tile
+  if (tid == 0) s_nh_max = 0;
   __syncthreads();
-  int n_t = 0, n_s = 0, n_h = 0;
+  int n_t = 0, n_s = 0, n_h = 0, nh_max = 0;
   if (has_e && cnt > 0) {
     n_t = (cnt + a.tn - 1) / a.tn;
     if (a.spi > 0) {
@@ -285,9 +287,11 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
         }
         n_s += ns;
         n_h += (ns + a.spi - 1) / a.spi;
+        nh_max = max(nh_max, (ns + a.spi - 1) / a.spi);
       }
     }
   }
+  if (nh_max > 0) atomicMax(&s_nh_max, nh_max);
   int tot_t, tot_s, tot_h, tbase, sbase, hbase;
   block_exclusive_scan3(n_t, n_s, n_h, warp_sums, tbase, sbase, hbase, tot_t, tot_s, tot_h);
   if (a.gu_cnt)   // the K-split gate_up's arrival counters, one per (tile, weight tile)
@@ -343,6 +347,7 @@ __device__ void align_tables(const AlignArgs& a, int* warp_sums, int* sb, bool w
     a.hdr->n_tiles = tot_t;
     a.hdr->n_slots = tot_s;
     a.hdr->n_shrink = tot_h * a.sks;
+    a.hdr->sh_max = s_nh_max * a.sks;   // (the scan above ended with a barrier)
     a.hdr->work[0] = 0;
     a.hdr->work[1] = 0;
   }

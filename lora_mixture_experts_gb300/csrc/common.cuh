@@ -45,7 +45,8 @@ struct WsHeader {
   int n_slots;       // LoRA slots
   int n_shrink;      // shrink items
   int work[2];       // items claimed so far by each GEMM phase (zeroed by the align)
-  int pad_[25];
+  int sh_max;        // most shrink entries (items x K splits) of any one tile
+  int pad_[24];
 };
 
 constexpr int kStatusBadIndex = MOELORA_ERR_BAD_INDEX;

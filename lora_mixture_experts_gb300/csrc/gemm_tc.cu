@@ -61,7 +61,8 @@ constexpr int kClaimAhead = 1;           // items claimed beyond those the produ
 // epilogue warps of the CTA.
 struct RingEntry {
   int w;
-  int pad_[3];
+  int sh;        // shrink entry of a shrink item, -1 for a main item
+  int pad_[2];
   TileInfo ti;
 };
 // K-block width and pipeline shape of CTA-pair tiles (the tensor-bound
@@ -130,46 +131,130 @@ struct Item {
   int ks;       // K split (main items)
 };
 
-// Item order: all shrink items first, then the main items, K split by K
-// split; inside a split, the token tiles' L2 groups in tile order.  A group is
-// a run of consecutive tiles of one expert (written by the align into each
-// tile's `grp`); inside it the weight tile m is the slow index and the tile
-// the fast one, so the tiles of an expert read each weight tile one after
-// the other while it is hot in L2, and the group's token rows (the align caps
-// the run length) stay resident across all m.  A group of tiles [g0, g0+gn)
-// holds the split's items [g0 * n_m, (g0 + gn) * n_m), so the group of a main
-// item is the group of tile w / n_m (its anchor).
-__device__ __forceinline__ int main_item_anchor(int w, int n_sh, int n_tiles, int n_m) {
-  w -= n_sh;
-  const int per_split = n_tiles * n_m;
-  return (w % per_split) / n_m;
+// Item order of a launch phase.  Main items come K split by K split; inside
+// a split, the token tiles' L2 groups in tile order.  A group is a run of
+// consecutive tiles of one expert (written by the align into each tile's
+// `grp`); inside it the weight tile m is the slow index and the tile the
+// fast one, so the tiles of an expert read each weight tile one after the
+// other while it is hot in L2, and the group's token rows (the align caps the
+// run length) stay resident across all m.
+//
+// Shrink entries come either all first (shs == 0), or, on CTA pairs whose
+// token rows exceed what L2 keeps, spread over the first split (shs > 0):
+// every tile gets shs shrink slots (its shrink entries, then empty slots that
+// the scheduler skips), placed `ahead` tiles before the tile itself.  The
+// first split is then a prologue of the slots of tiles [0, ahead) followed by
+// one block per group of tiles [g0, g0+gn): the slots of tiles [g0+ahead,
+// g0+gn+ahead) (none past the last tile), then the group's main items.  A
+// tile's shrink entries thus always come before its main items, about one
+// wave of items earlier: they are done when the main items' expand needs
+// their result, and the token rows they read are still in L2 when the main
+// items read them (all shrink entries first
+// made every main item re-read its rows from DRAM: +90 MB per projection on
+// the prefill batch).  Since block sizes are proportional to tile counts, the
+// group of a first-split item w is the group of tile (w - prologue) / (n_m +
+// shs), or (later splits) of tile w / n_m: its anchor.
+struct ItemOrder {
+  int n_sh;      // shrink entries
+  int n_tiles;
+  int n_m;       // weight tiles
+  int shs;       // shrink slots per tile, 0: all shrink entries first
+  int ahead;     // tiles by which a tile's shrink slots precede it (shs > 0)
+};
+
+__device__ __forceinline__ void group_of(int grp, int& g0, int& gn) {
+  g0 = grp >> 8;
+  gn = max(1, grp & 255);
 }
 
-// `grp`: the group of the item's tile (any tile of the group; ignored for
-// shrink items).
-__device__ __forceinline__ Item decode_item(int w, int n_sh, int n_tiles, int n_m, int grp,
-                                            const ShrinkItem* sh) {
+// Main item w of the order, given the group of its tile (any tile's `grp` in it).
+__device__ __forceinline__ Item decode_main(int w, const ItemOrder& o, int grp) {
   Item it;
-  if (w < n_sh) {
-    it.shrink = 1;
-    it.sh = w;
-    it.tile = sh[w].tile;
-    it.m = 0;
-    it.ks = 0;
+  int g0, gn;
+  group_of(grp, g0, gn);
+  const int per_split = o.n_tiles * o.n_m;
+  it.shrink = 0;
+  it.sh = -1;
+  if (o.shs > 0) {
+    const int pro = o.ahead * o.shs;
+    const int region0 = pro + o.n_tiles * (o.n_m + o.shs);
+    if (w < region0) {
+      const int wm = w - pro - g0 * (o.n_m + o.shs) - gn * o.shs;
+      it.ks = 0;
+      it.m = wm / gn;
+      it.tile = g0 + (wm - it.m * gn);
+      return it;
+    }
+    w -= region0;
+    it.ks = 1 + w / per_split;
+    w -= (it.ks - 1) * per_split;
   } else {
-    w -= n_sh;
-    const int per_split = n_tiles * n_m;
+    w -= o.n_sh;
     it.ks = w / per_split;
     w -= it.ks * per_split;
-    const int g0 = grp >> 8;
-    const int gn = max(1, grp & 255);
-    const int wl = w - g0 * n_m;
-    it.shrink = 0;
-    it.sh = -1;
-    it.m = wl / gn;
-    it.tile = g0 + (wl - it.m * gn);
   }
+  const int wl = w - g0 * o.n_m;
+  it.m = wl / gn;
+  it.tile = g0 + (wl - it.m * gn);
   return it;
+}
+
+// The scheduler's view of item w: a shrink entry (sh >= 0, tile = its tile),
+// a main item (sh = -1, tile = its tile), or an empty shrink slot (false).
+__device__ __forceinline__ bool resolve_item(int w, const ItemOrder& o, const TileInfo* tiles,
+                                             const ShrinkItem* shrink, int sks, int& sh, int& tile) {
+  const int per_split = o.n_tiles * o.n_m;
+  auto slot = [&](int t, int j) -> bool {
+    if (t >= o.n_tiles) return false;
+    const TileInfo& ti = tiles[t];
+    if (j >= ti.nsh * sks) return false;
+    sh = ti.sh_base + j;
+    tile = t;
+    return true;
+  };
+  int grp;
+  if (o.shs > 0) {
+    const int pro = o.ahead * o.shs;
+    const int region0 = pro + o.n_tiles * (o.n_m + o.shs);
+    if (w < pro) return slot(w / o.shs, w % o.shs);
+    if (w < region0) {
+      const int w2 = w - pro;
+      grp = tiles[w2 / (o.n_m + o.shs)].grp;
+      int g0, gn;
+      group_of(grp, g0, gn);
+      const int wl = w2 - g0 * (o.n_m + o.shs);
+      if (wl < gn * o.shs) return slot(g0 + wl / o.shs + o.ahead, wl % o.shs);
+    } else {
+      grp = tiles[((w - region0) % per_split) / o.n_m].grp;
+    }
+  } else {
+    if (w < o.n_sh) {
+      sh = w;
+      tile = shrink[w].tile;
+      return true;
+    }
+    grp = tiles[((w - o.n_sh) % per_split) / o.n_m].grp;
+  }
+  sh = -1;
+  tile = decode_main(w, o, grp).tile;
+  return true;
+}
+
+// A consumer's view of item w, from its ring entry: the shrink entry `sh`
+// (spread order only; all first, shrink item w is entry w), the tile's group.
+__device__ __forceinline__ Item item_of(int w, int sh, const ItemOrder& o, int grp,
+                                        const ShrinkItem* shrink) {
+  if (o.shs == 0) sh = w < o.n_sh ? w : -1;
+  if (sh >= 0) {
+    Item it;
+    it.shrink = 1;
+    it.sh = sh;
+    it.tile = shrink[sh].tile;
+    it.m = 0;
+    it.ks = 0;
+    return it;
+  }
+  return decode_main(w, o, grp);
 }
 
 // First K chunk of a main item's loop.  Concurrent items start at different
@@ -213,7 +298,7 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
 // running CTAs, so the gate_up items waited for were claimed earlier by
 // running CTAs and the wait ends.  NPH is a template argument so
 // that the one-phase kernel reads its parameters at fixed offsets.
-template <int TN, bool PAIR, int NPH>
+template <int TN, bool PAIR, int NPH, bool SPREAD>
 __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps& maps1,
                                           const GemmParams& p0, const GemmParams& p1) {
   constexpr int n_phases = NPH;
@@ -313,7 +398,18 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
 
   const int n_tiles = p.hdr->n_tiles;
   const int n_sh = p.r > 0 ? p.hdr->n_shrink : 0;
-  const int items0 = n_sh + n_tiles * p0.n_mtiles * p0.ksplit;
+  // CTA pairs interleave the shrink items with the first split's groups (the
+  // two-phase launch runs on single-CTA tiles only)
+  // (a tile's shrink slots come one wave of items before its main items:
+  // `ahead` tiles of n_m weight tiles each cover the launch's work units)
+  const int shs = PAIR && SPREAD && n_sh > 0 ? min(p.hdr->sh_max, n_sh) : 0;
+  const int units = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  const int ahead = shs > 0 ? min(n_tiles, max(1, (units + p0.n_mtiles - 1) / p0.n_mtiles)) : 0;
+  const ItemOrder ord0{n_sh, n_tiles, p0.n_mtiles, shs, ahead};
+  const ItemOrder ord1{n_sh, n_tiles, p1.n_mtiles, 0, 0};
+  const int items0 = shs > 0 ? ahead * shs + n_tiles * (p0.n_mtiles + shs) +
+                                   n_tiles * p0.n_mtiles * (p0.ksplit - 1)
+                             : n_sh + n_tiles * p0.n_mtiles * p0.ksplit;
   const int n_items = items0 + (n_phases > 1 ? n_sh + n_tiles * p1.n_mtiles * p1.ksplit : 0);
   const int spc = p.r > 0 ? 128 / p.r : 0;    // shrink slots per CTA
   // shrink completions a tile's item waits for: every CTA of the item signals
@@ -337,10 +433,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
   };
   // Consume ring entry qc (single-thread consumers: producer, MMA issuer):
   // wait until it is written, copy it, release the slot.
-  auto ring_take = [&](uint32_t qc, int& w, TileInfo& ti, bool producer) -> bool {
+  auto ring_take = [&](uint32_t qc, int& w, int& sh, TileInfo& ti, bool producer) -> bool {
     const int q = static_cast<int>(qc % kQ);
     if (!entry_written(q, (qc / kQ) & 1)) return false;
     w = ring[q].w;
+    sh = ring[q].sh;
     ti = ring[q].ti;
     entry_release(q);
     if (producer && leader) mbar_arrive(smem_u32(&itemp_bar[q]));
@@ -453,15 +550,14 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         }
       };
       for (uint32_t qc = 0; ok; ++qc) {
-        int w;
+        int w, wsh;
         TileInfo ti;
-        if (!(ok = ring_take(qc, w, ti, true))) break;
+        if (!(ok = ring_take(qc, w, wsh, ti, true))) break;
         if (w < 0) break;
         const int ph = NPH == 2 && w >= items0 ? 1 : 0;
         const GemmParams& p = NPH == 2 && ph ? p1 : p0;
         const GemmMaps& maps = NPH == 2 && ph ? maps1 : maps0;
-        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, ti.grp,
-                                    p.shrink);
+        const Item it = item_of(w - (ph ? items0 : 0), wsh, ph ? ord1 : ord0, ti.grp, p.shrink);
         const int nk = (p.K + C::kBK - 1) / C::kBK;   // K blocks of the base GEMM
         const bool gate_up = p.mode == kModeGateUp;
         if (p.act_wait) {
@@ -626,14 +722,13 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
       bool ok = true;
       bool issued = false;
       for (uint32_t qc = 0; ok; ++qc, ++li) {
-        int w;
+        int w, wsh;
         TileInfo ti;
-        if (!(ok = ring_take(qc, w, ti, false))) break;
+        if (!(ok = ring_take(qc, w, wsh, ti, false))) break;
         if (w < 0) break;
         const int ph = NPH == 2 && w >= items0 ? 1 : 0;
         const GemmParams& p = NPH == 2 && ph ? p1 : p0;
-        const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, ti.grp,
-                                    p.shrink);
+        const Item it = item_of(w - (ph ? items0 : 0), wsh, ph ? ord1 : ord0, ti.grp, p.shrink);
         const int nk = (p.K + C::kBK - 1) / C::kBK;
         const int nmma = (ti.nrows + 15) & ~15;
         const uint32_t idesc = make_idesc_bf16(nmma, PAIR ? 256 : 128);
@@ -762,22 +857,33 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
           const uint32_t e = qp - kClaimAhead;
           if (!(ok = mbar_wait(smem_u32(&itemp_bar[e % kQ]), (e / kQ) & 1, abort_flag))) break;
         }
-        int w = atomicAdd(p.work_ctr, 1);
-        if (w >= n_items) w = -1;
+        int w, wsh = -1;
         TileInfo ti = {};
-        if (w >= 0) {
+        for (;;) {
+          w = atomicAdd(p.work_ctr, 1);
+          if (w >= n_items) {
+            w = -1;
+            break;
+          }
           const bool w1 = NPH == 2 && w >= items0;
           const GemmParams& pw = w1 ? p1 : p0;
-          const int wl = w - (w1 ? items0 : 0);
-          const int grp = wl < n_sh ? 0 : p.tiles[main_item_anchor(wl, n_sh, n_tiles, pw.n_mtiles)].grp;
-          ti = p.tiles[decode_item(wl, n_sh, n_tiles, pw.n_mtiles, grp, p.shrink).tile];
+          int tile;
+          // (an empty shrink slot of the spread order: claim the next item)
+          if (resolve_item(w - (w1 ? items0 : 0), w1 ? ord1 : ord0, p.tiles, p.shrink, pw.sh_splits, wsh,
+                           tile)) {
+            ti = p.tiles[tile];
+            break;
+          }
         }
         ring[q].ti = ti;
         ring[q].w = w;
+        ring[q].sh = wsh;
         if (PAIR) {
           // the peer's copy of the entry, released by its "written" arrive
           const uint32_t dst = peer_ring + q * static_cast<uint32_t>(sizeof(RingEntry));
           st_cluster_u32(dst, static_cast<uint32_t>(w));
+          if (shs > 0)   // (all shrink entries first: the peer decodes them from w)
+            st_cluster_u32(dst + static_cast<uint32_t>(offsetof(RingEntry, sh)), static_cast<uint32_t>(wsh));
           const uint32_t* tv = reinterpret_cast<const uint32_t*>(&ti);
 #pragma unroll
           for (int i = 0; i < static_cast<int>(sizeof(TileInfo) / 4); ++i)
@@ -810,14 +916,14 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
         break;
       }
       const int w = ring[q].w;
+      const int wsh = ring[q].sh;
       const TileInfo ti = ring[q].ti;
       __syncwarp();
       if (lane == 0) entry_release(q);
       if (w < 0) break;
       const int ph = NPH == 2 && w >= items0 ? 1 : 0;
       const GemmParams& p = NPH == 2 && ph ? p1 : p0;
-      const Item it = decode_item(w - (ph ? items0 : 0), n_sh, n_tiles, p.n_mtiles, ti.grp,
-                                  p.shrink);
+      const Item it = item_of(w - (ph ? items0 : 0), wsh, ph ? ord1 : ord0, ti.grp, p.shrink);
       const bool gate_up = p.mode == kModeGateUp;
       const int nmma = (ti.nrows + 15) & ~15;
       const int buf = li & 1;
@@ -1113,10 +1219,12 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
 }
 
 // One phase per launch: the parameters by value, read at fixed offsets.
-template <int TN, bool PAIR>
+// SPREAD: the shrink entries spread over the first K split (CTA pairs; a
+// separate instance, so that the all-first order keeps its own code).
+template <int TN, bool PAIR, bool SPREAD>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  gemm_body<TN, PAIR, 1>(maps, maps, p, p);
+  gemm_body<TN, PAIR, 1, SPREAD>(maps, maps, p, p);
 }
 
 // Both phases in one launch (single-CTA tiles): the items pick their phase's
@@ -1127,19 +1235,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                               const __grid_constant__ GemmMaps maps1,
                               const __grid_constant__ GemmParams p0,
                               const __grid_constant__ GemmParams p1) {
-  gemm_body<TN, false, 2>(maps0, maps1, p0, p1);
+  gemm_body<TN, false, 2, false>(maps0, maps1, p0, p1);
 }
 
-template <int TN, bool PAIR, int NPH>
+template <int TN, bool PAIR, int NPH, bool SPREAD>
 struct KernelOf {
-  static constexpr auto fn = moe_gemm_kernel<TN, PAIR>;
+  static constexpr auto fn = moe_gemm_kernel<TN, PAIR, SPREAD>;
 };
 template <int TN>
-struct KernelOf<TN, false, 2> {
+struct KernelOf<TN, false, 2, false> {
   static constexpr auto fn = moe_gemm_two_phase_kernel<TN>;
 };
 
-template <int TN, bool PAIR, int NPH>
+template <int TN, bool PAIR, int NPH, bool SPREAD = false>
 cudaError_t launch_tn(const GemmMaps& maps0, const GemmParams& p0, const GemmMaps& maps1,
                       const GemmParams& p1, int grid, cudaStream_t stream) {
   using C = Cfg<TN, PAIR>;
@@ -1149,7 +1257,7 @@ cudaError_t launch_tn(const GemmMaps& maps0, const GemmParams& p0, const GemmMap
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(KernelOf<TN, PAIR, NPH>::fn,
+    cudaError_t e = cudaFuncSetAttribute(KernelOf<TN, PAIR, NPH, SPREAD>::fn,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1166,12 +1274,12 @@ cudaError_t launch_tn(const GemmMaps& maps0, const GemmParams& p0, const GemmMap
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, KernelOf<TN, PAIR, NPH>::fn, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&clusters, KernelOf<TN, PAIR, NPH, SPREAD>::fn, &cfg);
       if (e != cudaSuccess) return e;
       max_units = clusters;
     } else {
       int per_sm = 0, sms = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KernelOf<TN, PAIR, NPH>::fn, kThreads,
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KernelOf<TN, PAIR, NPH, SPREAD>::fn, kThreads,
                                                         C::kSmemBytes);
       if (e != cudaSuccess) return e;
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1202,9 +1310,9 @@ cudaError_t launch_tn(const GemmMaps& maps0, const GemmParams& p0, const GemmMap
   cfg.attrs = attr;
   cfg.numAttrs = na;
   if constexpr (NPH == 2)
-    return cudaLaunchKernelEx(&cfg, KernelOf<TN, PAIR, NPH>::fn, maps0, maps1, p0, p1);
+    return cudaLaunchKernelEx(&cfg, KernelOf<TN, PAIR, NPH, SPREAD>::fn, maps0, maps1, p0, p1);
   else
-    return cudaLaunchKernelEx(&cfg, KernelOf<TN, PAIR, NPH>::fn, maps0, p0);
+    return cudaLaunchKernelEx(&cfg, KernelOf<TN, PAIR, NPH, SPREAD>::fn, maps0, p0);
 }
 
 }  // namespace
@@ -1232,7 +1340,9 @@ int moe_gemm_stage_kblocks(int tn) {
 
 cudaError_t launch_moe_gemm(int tn, const GemmMaps& maps, const GemmParams& p, int grid,
                             cudaStream_t stream) {
-  if (tn == 256) return launch_tn<256, true, 1>(maps, p, maps, p, grid, stream);
+  if (tn == 256)
+    return p.spread_shrink ? launch_tn<256, true, 1, true>(maps, p, maps, p, grid, stream)
+                           : launch_tn<256, true, 1, false>(maps, p, maps, p, grid, stream);
   if (tn == 128) return launch_tn<128, false, 1>(maps, p, maps, p, grid, stream);
   if (tn == 64) return launch_tn<64, false, 1>(maps, p, maps, p, grid, stream);
   if (tn == 32) return launch_tn<32, false, 1>(maps, p, maps, p, grid, stream);

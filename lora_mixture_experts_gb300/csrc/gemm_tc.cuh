@@ -87,6 +87,8 @@ struct GemmParams {
   int* gu_cnt;
   int gu_slots;
   int* work_ctr;        // items claimed so far (zeroed by the align); NULL = fixed shares
+  int spread_shrink;    // 1: on CTA pairs, spread the shrink entries over the first K split
+                        //    (set when the launch's token rows are too large to stay in L2)
   int early_weights;    // 1: on unpaired tiles, stream the first weight blocks before
                         //    the preceding launch has finished (see the kernel)
 };

@@ -718,6 +718,17 @@ void fill_gemm_tables(const Plan& p, void* ws, AlignArgs& a) {
   a.gu_nm = p.gksplit > 1 ? (p.I + 63) / 64 : 0;
 }
 
+// Spread a CTA-pair launch's shrink entries over its first K split (see the
+// GEMM's item order) when its token rows, n rows of K bf16, are more than L2
+// keeps across the launch's weight stream (measured on the GB300: the prefill
+// batch's 94 MB of rows per projection, then read from DRAM once instead of
+// twice; the skewed batch's 13 and 34 MB and the dense T = 512 linear's 8 MB
+// gain nothing and lose 0.3-1% to the later shrink).
+int spread_shrink(long long n_rows, int K) {
+  if (const char* v = std::getenv("MOELORA_SPREAD_SHRINK")) return std::atoi(v) != 0 ? 1 : 0;
+  return static_cast<double>(n_rows) * K * 2.0 > 64.0 * (1 << 20) ? 1 : 0;
+}
+
 GemmParams gemm_params(const Plan& p, void* ws, const AlignArgs& a) {
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
@@ -902,6 +913,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   GemmParams gu = gemm_params(p, ws, a);
   gu.mode = kModeGateUp;
   gu.K = p.H;
+  gu.spread_shrink = spread_shrink(p.n, gu.K);
   set_splits(gu, p.gksplit, gu.K, static_cast<int>(bk));
   if (p.gksplit > 1) {
     gu.gu_part = ws_ptr<float>(ws, p.off_gupart);
@@ -921,6 +933,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
   GemmParams gd = gemm_params(p, ws, a);
   gd.mode = kModeDown;
   gd.K = p.I;
+  gd.spread_shrink = spread_shrink(p.n, gd.K);
   gd.n_mtiles = (p.H + (paired ? 255 : 127)) / (paired ? 256 : 128);
   gd.out_feats = p.H;
   gd.done_target = 2;
@@ -1074,6 +1087,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
 
   GemmParams g = gemm_params(p, ws, a);
   g.K = p.H;
+  g.spread_shrink = spread_shrink(p.n, g.K);
   const bool paired = moe_gemm_paired(p.tn);
   g.n_mtiles = (p.N + (paired ? 255 : 127)) / (paired ? 256 : 128);
   g.out_feats = p.N;

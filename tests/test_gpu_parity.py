@@ -281,6 +281,56 @@ def test_forward_gate_up_split_k(monkeypatch, shape, splits, two_phase):
     assert torch.equal(out, again)          # the order of arrival does not matter
 
 
+# CTA-pair shapes for the spread shrink order: ragged tiles, several per
+# expert, tiles with more adapters than one shrink item stacks and tiles
+# with none (adapter -1), every rank
+SPREAD_SHAPES = [(700, 512, 384, 3, 2, 6, 16), (520, 256, 512, 5, 3, 9, 32), (300, 384, 256, 2, 1, 3, 64),
+                 (900, 192, 320, 7, 2, 12, 48)]
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("shape", SPREAD_SHAPES,
+                         ids=[f"T{s[0]}_H{s[1]}_I{s[2]}_E{s[3]}_k{s[4]}_L{s[5]}_r{s[6]}" for s in SPREAD_SHAPES])
+def test_forward_spread_shrink_order(monkeypatch, shape, splits):
+    """CTA-pair launches with the shrink entries spread over the first K
+    split (forced here; the built-in choice spreads them only when the token
+    rows are more than L2 keeps): each tile's shrink slots, empty ones
+    included, a wave of items ahead of its main items.  Compared with the
+    oracle, and bit for bit with the all-first order: the claim order
+    changes no sum."""
+    monkeypatch.setenv("MOELORA_TN", "256")
+    monkeypatch.setenv("MOELORA_SHRINK_SPLITS", str(splits))
+    T, H, I, E, k, L, r = shape
+    d = make_moe_case(small_moe_case(T, H, I, E, k, L, r), seed=41, device=DEV)
+    monkeypatch.setenv("MOELORA_SPREAD_SHRINK", "1")
+    out = _run_parity(d, what=f"{shape} spread shrink, {splits} shrink splits")
+    monkeypatch.setenv("MOELORA_SPREAD_SHRINK", "0")
+    assert torch.equal(out, _gpu_forward(d))
+
+
+@pytest.mark.parametrize("spread", ["0", "1"])
+def test_linear_spread_shrink_order(monkeypatch, spread):
+    """The dense linear on CTA pairs with its shrink entries spread over the
+    first K split and all first: the same bits, and the oracle's result."""
+    monkeypatch.setenv("MOELORA_TN", "256")
+    monkeypatch.setenv("MOELORA_SPREAD_SHRINK", spread)
+    g = torch.Generator(device=DEV).manual_seed(43)
+    T, K, N, L, r = 777, 512, 640, 9, 16
+    x = torch.randn(T, K, generator=g, device=DEV).bfloat16()
+    W = (torch.randn(N, K, generator=g, device=DEV) * K ** -0.5).bfloat16()
+    A = (torch.randn(L, r, K, generator=g, device=DEV) * K ** -0.5).bfloat16()
+    B = (torch.randn(L, N, r, generator=g, device=DEV) * r ** -0.5).bfloat16()
+    lo = torch.randint(-1, L, (T,), generator=g, device=DEV).int()
+    out = binding.moe_lora_linear(x, lo, W, A, B)
+    n = np_inputs({"x": x, "W": W, "A": A, "B": B})
+    exp = ref.moe_lora_linear_ref(n["x"], lo.cpu().numpy(), n["W"], n["A"], n["B"])
+    ok, msg = compare(out, exp, f"linear spread={spread}")
+    print(msg)
+    assert ok, msg
+    monkeypatch.setenv("MOELORA_SPREAD_SHRINK", "1" if spread == "0" else "0")
+    assert torch.equal(out, binding.moe_lora_linear(x, lo, W, A, B))
+
+
 @pytest.mark.parametrize("shape", _random_shapes(24, 17), ids=lambda s: "T{T}_H{H}_I{I}_E{E}_k{k}_L{L}_r{r}".format(**s))
 def test_forward_random_shapes(shape):
     s = shape
