@@ -837,10 +837,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps0, const GemmMaps&
     // the tail (decode 0.266 -> 0.261 ms, dense T=1 0.103 -> 0.094 ms on
     // GB300).  On CTA pairs the leader claims for the pair and writes the
     // peer's ring entry as well (the peer's scheduler has nothing to do).
-    // Items are claimed in index order by CTAs that are running, so shrink
-    // items are always claimed, and finished, by resident CTAs before any
-    // main item that waits for them: no wait depends on a CTA (pair) that
-    // has not started, however many of the grid's CTAs are resident.
+    // Items are claimed in index order by CTAs that are running, and a
+    // tile's shrink items precede its main items in either order, so they
+    // are always claimed, and finished, by resident CTAs before any main item
+    // that waits for them: no wait depends on a CTA (pair) that has not
+    // started, however many of the grid's CTAs are resident.
     if (lane == 0 && leader) {
       bool ok = true;
       const uint32_t peer_ring = PAIR ? mapa_shared(smem_u32(ring), 1) : 0;

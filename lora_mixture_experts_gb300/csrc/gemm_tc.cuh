@@ -93,7 +93,7 @@ struct GemmParams {
                         //    the preceding launch has finished (see the kernel)
 };
 
-// Launches one GEMM phase (shrink items first, then the main items) as a
+// Launches one GEMM phase (a tile's shrink items before its main items) as a
 // persistent kernel on up to `grid` work units (CTAs, or CTA pairs for
 // paired tiles), capped at what can be resident at once.  tn is 16, 32, 64,
 // 128 or 256.
