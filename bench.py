@@ -359,8 +359,8 @@ def measure(case, args, steps, warmup, rank, world, device, peaks, sampler, e2e=
         ws = binding.alloc_workspace(binding.moelora_linear_workspace_bytes(dims), device)
         out = torch.empty((case.T, case.N), dtype=torch.bfloat16, device=device)
 
-        def fwd(x=d["x"], lo=d["lora_ids"]):
-            binding.moe_lora_linear(x, lo, d["W"], d["A"], d["B"], out=out, ws=ws)
+        def fwd(x=d["x"], lo=d["lora_ids"], o=None):
+            binding.moe_lora_linear(x, lo, d["W"], d["A"], d["B"], out=out if o is None else o, ws=ws)
         layer = roofline.linear_work(d["lora_ids"].cpu().numpy(), case.K, case.N, case.r)
         kernel_work = {"gemm_linear": layer}
         step_inputs = ["x", "lora_ids"]
@@ -369,9 +369,9 @@ def measure(case, args, steps, warmup, rank, world, device, peaks, sampler, e2e=
         ws = binding.alloc_workspace(binding.moelora_workspace_bytes(dims), device)
         out = torch.empty_like(d["x"])
 
-        def fwd(x=d["x"], ids=d["topk_ids"], w=d["topk_weights"], lo=d["lora_ids"]):
+        def fwd(x=d["x"], ids=d["topk_ids"], w=d["topk_weights"], lo=d["lora_ids"], o=None):
             binding.moe_lora_forward(x, ids, w, lo, d["W_gate_up"], d["W_down"], d["A_gu"], d["B_gu"],
-                                     d["A_d"], d["B_d"], out=out, ws=ws)
+                                     d["A_d"], d["B_d"], out=out if o is None else o, ws=ws)
         layer, gu, dn = roofline.moe_layer_work(d["topk_ids"].cpu().numpy(), d["lora_ids"].cpu().numpy(),
                                                 case.H, case.I, case.r)
         # single-CTA tiles run both projections in one launch
@@ -479,41 +479,68 @@ def measure(case, args, steps, warmup, rank, world, device, peaks, sampler, e2e=
         "clocks": clocks,
     }
     if e2e:
-        # end to end through the public API: the step's inputs packed in one
-        # pinned host buffer (each at a 256-byte offset) and copied in one
-        # transfer, the forward on device views of that buffer, the result
-        # read back, every step
+        # end to end through the public API, as a serving loop runs it: every
+        # step copies its inputs from pinned host memory (packed in one
+        # buffer, each at a 256-byte offset, one transfer) and reads its
+        # result back.  The copies run on their own streams, into and out of
+        # double buffers, so that step n+1's inputs arrive and step n-1's
+        # result leaves while step n computes; events order every buffer's
+        # reuse after the work that last read it.
         offs, nbytes = {}, 0
         for k in step_inputs:
             offs[k] = nbytes
             nbytes += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
-        host_buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-        dev_buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
         def view(buf, k):
             n = d[k].numel() * d[k].element_size()
             return buf[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
-        for k in step_inputs:
-            view(host_buf, k).copy_(d[k].cpu())
-        dev_in = {k: view(dev_buf, k) for k in step_inputs}
-        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        host_buf = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        dev_buf = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(2)]
+        for b in range(2):
+            for k in step_inputs:
+                view(host_buf[b], k).copy_(d[k].cpu())
+        dev_in = [{k: view(dev_buf[b], k) for k in step_inputs} for b in range(2)]
+        out_d = [out, torch.empty_like(out)]
+        out_h = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+        compute = torch.cuda.current_stream()
+        h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "fwd", "out")}
+        used = [False, False]
 
-        def e2e_step():
-            dev_buf.copy_(host_buf, non_blocking=True)
-            fwd(*[dev_in[k] for k in step_inputs])
-            out_h.copy_(out, non_blocking=True)
-        for _ in range(min(warmup, 5)):
-            e2e_step()
+        def e2e_step(n):
+            b = n & 1
+            if used[b]:
+                h2d.wait_event(ev["fwd"][b])          # step n-2 read dev_buf[b]
+            with torch.cuda.stream(h2d):
+                dev_buf[b].copy_(host_buf[b], non_blocking=True)
+            ev["in"][b].record(h2d)
+            compute.wait_event(ev["in"][b])
+            if used[b]:
+                compute.wait_event(ev["out"][b])      # step n-2's result left out_d[b]
+            fwd(*[dev_in[b][k] for k in step_inputs], o=out_d[b])
+            ev["fwd"][b].record(compute)
+            d2h.wait_event(ev["fwd"][b])
+            with torch.cuda.stream(d2h):
+                out_h[b].copy_(out_d[b], non_blocking=True)
+            ev["out"][b].record(d2h)
+            used[b] = True
+        for n in range(min(warmup, 5)):
+            e2e_step(n)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
-        for _ in range(K):
-            e2e_step()
+        for n in range(K):
+            e2e_step(n)
         torch.cuda.synchronize()
         e2e_s = reduce_max((time.perf_counter() - t0) / K, world, device)
         res["e2e"] = {"value": case.T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
-                      "d2h_bytes_per_step": out.numel() * out.element_size()}
+                      "d2h_bytes_per_step": out.numel() * out.element_size(),
+                      "pipeline": "copies on two streams, double-buffered, overlapping the next and "
+                                  "previous steps' compute"}
+        # the read-back is this step's result: compare it with the device output
+        if not torch.equal(out_h[(K - 1) & 1], out_d[(K - 1) & 1].cpu()):
+            raise RuntimeError(f"{case.name}: the end-to-end read-back differs from the device output")
     # the last timed call's output is the forward of these inputs again
     fwd()
     torch.cuda.synchronize()
