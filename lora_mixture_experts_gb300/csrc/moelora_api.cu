@@ -273,6 +273,9 @@ void plan_gemm_tables(Plan& p, Bump& b) {
   if (t_tn) p.tn = t_tn;
   if (const int f = env_override("MOELORA_TN", 16, 256))
     if (f == 16 || f == 32 || f == 64 || f == 128 || f == 256) p.tn = f;
+  // (a tile's L2 group is packed as first tile * 256 + length into one int,
+  // so fewer than 2^23 tiles: 256-row tiles always give that, T * k < 2^30)
+  if (static_cast<long long>(p.n) / p.tn + p.E + 1 >= (1ll << 23)) p.tn = 256;
   p.n_tiles_max = p.n / p.tn + std::min(p.E, std::max(p.n, 1)) + 1;
   p.n_slots_max = p.lora ? std::min(p.n, p.E * p.L + p.n_tiles_max) : 0;
   p.n_sh_max = p.n_slots_max;
