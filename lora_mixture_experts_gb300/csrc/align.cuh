@@ -70,6 +70,14 @@ struct AlignArgs {
   const uint4* x;
   uint4* x_perm;
   int hv;
+  // L2 prefetch by extra CTAs of the small align (pf_ctas > 0): the weight
+  // rows that the first GEMM phase streams first, which are its routed
+  // experts' weights in expert order, pf_expert_bytes each (16-byte
+  // multiples from pf_base), up to pf_bytes, while the tables are built
+  const unsigned char* pf_base;
+  long long pf_expert_bytes;
+  long long pf_bytes;
+  int pf_ctas;
 };
 
 // The three align kernels; hist and scatter are skipped (return success)

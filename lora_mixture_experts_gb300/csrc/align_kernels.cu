@@ -383,6 +383,44 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
   align_tables(a, warp_sums, sb);
 }
 
+// Weight prefetch of the small align: CTA pi of n_pf counts the entries of
+// each expert, ranks the routed experts in expert order (the order of their
+// token tiles, and so of the first GEMM phase's main items), and issues its
+// share of 64 KB L2 prefetches over the first routed experts' weights, up to
+// pf_bytes.  The copies run in the memory system while the align's other
+// CTAs build the tables, so the GEMM's first items read them from L2 instead
+// of HBM, which the align leaves idle.  Nothing is written; the CTA returns.
+__device__ void align_prefetch(const AlignArgs& a, int* warp_sums, int* cnt, int pi, int n_pf) {
+  __shared__ int s_list[8];   // routed experts, in order, whose bytes are prefetched
+  const int tid = threadIdx.x;
+  for (int e = tid; e < a.E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int f = tid; f < a.n; f += blockDim.x) {
+    const int e = a.topk_ids ? a.topk_ids[f] : 0;
+    if (e >= 0 && e < a.E) cnt[e] = 1;   // (a flag: any entry makes the expert routed)
+  }
+  __syncthreads();
+  const bool routed = tid < a.E && cnt[tid] > 0;
+  int n_routed;
+  const int rank = block_exclusive_scan(routed ? 1 : 0, warp_sums, &n_routed);
+  const long long eb = a.pf_expert_bytes;
+  const int n_list = static_cast<int>(min(static_cast<long long>(min(n_routed, 8)), (a.pf_bytes + eb - 1) / eb));
+  if (routed && rank < n_list) s_list[rank] = tid;
+  __syncthreads();
+  const long long total = min(a.pf_bytes, n_list * eb) & ~15ll;
+  constexpr long long kChunk = 1 << 16;
+  const long long n_chunks = (total + kChunk - 1) / kChunk;
+  for (long long c = pi + static_cast<long long>(n_pf) * tid; c < n_chunks;
+       c += static_cast<long long>(n_pf) * blockDim.x) {
+    const long long off = c * kChunk;
+    const int li = static_cast<int>(off / eb);
+    const long long o = off - li * eb;
+    const long long bytes = min(min(kChunk, eb - o), total - off);
+    if (bytes >= 16)
+      prefetch_l2_bulk(a.pf_base + static_cast<long long>(s_list[li]) * eb + o, static_cast<uint32_t>(bytes & ~15ll));
+  }
+}
+
 // The whole align in one CTA for up to kScanThreads entries (decode-sized
 // batches), launched with max(entries, experts) threads rounded to a warp:
 // bins, stable in-bin ranks (the warps holding entries take turns in entry
@@ -405,6 +443,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) align_small_kernel(AlignArgs 
     if (tid == 0) a.hdr->err = 0;
     __syncthreads();
   }
+  // the last pf_ctas CTAs prefetch weights (no router here: the ids are inputs)
+  const int n_pf = a.pf_ctas > 0 && a.pf_base && !a.logits ? a.pf_ctas : 0;
+  if (static_cast<int>(blockIdx.x) >= static_cast<int>(gridDim.x) - n_pf) {
+    align_prefetch(a, warp_sums, sm_bins, static_cast<int>(blockIdx.x) - (static_cast<int>(gridDim.x) - n_pf),
+                   n_pf);
+    return;
+  }
+  const int gx = static_cast<int>(gridDim.x) - n_pf;   // the table and copying CTAs
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int f = tid;
@@ -462,12 +508,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) align_small_kernel(AlignArgs 
       }
     }
   }
-  if (gather && (gridDim.x == 1 || !tables)) {
+  if (gather && (gx == 1 || !tables)) {
     // rows of the entries, 16-byte pieces spread over the copying CTAs
     // (CTAs 1.. when there are several); padding rows are not written
     __syncthreads();
-    const int copiers = gridDim.x > 1 ? static_cast<int>(gridDim.x) - 1 : 1;
-    const int ci = gridDim.x > 1 ? static_cast<int>(blockIdx.x) - 1 : 0;
+    const int copiers = gx > 1 ? gx - 1 : 1;
+    const int ci = gx > 1 ? static_cast<int>(blockIdx.x) - 1 : 0;
     // (a thread's pieces are loaded together, then stored: four row reads in
     // flight instead of one after another; on the decode batch the copying
     // CTAs' row copy took 3.1 us, now 1.7 us, and the call 238.2 -> 237.1 us)
@@ -693,6 +739,7 @@ cudaError_t launch_align_small(const AlignArgs& a, cudaStream_t stream, bool cha
     grid = 1 + static_cast<int>(std::min<long long>((pieces + 4LL * threads - 1) / (4LL * threads),
                                                     std::max(1, num_sms - 1)));
   }
+  if (a.pf_ctas > 0 && a.pf_base && !a.logits) grid += a.pf_ctas;   // the prefetching CTAs
   const size_t smem = (static_cast<size_t>(a.nbins) + (gather ? a.n : 0)) * sizeof(int);
   return launch_chained(align_small_kernel, dim3(grid), dim3(threads), smem, stream, chained, b);
 }

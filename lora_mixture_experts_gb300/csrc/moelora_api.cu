@@ -612,6 +612,27 @@ struct Launcher {
 // *gathered tells the caller whether it did.
 constexpr size_t kFusedGatherBytes = 512 * 1024;
 
+// L2 prefetch by extra CTAs of the small align (see align_prefetch) of the
+// weights that the first GEMM phase streams first: its routed experts' whole
+// weights in expert order, which is what that phase reads first when it
+// does not split K.  Budget and CTAs measured on the GB300 (decode 237.0 ->
+// 236.1 us, dense MLP T = 64 189.2 -> 188.3 us with 16 MB over 32 CTAs; 40
+// and 80 MB were slower than none: the prefetch then competes with the
+// GEMM's own first loads).  MOELORA_PF_MB / MOELORA_PF_CTAS override them
+// (0 turns the prefetch off).
+void set_prefetch(AlignArgs& a, const void* w, long long expert_bytes, bool ok) {
+  a.pf_ctas = 0;
+  const char* mb_env = std::getenv("MOELORA_PF_MB");
+  const char* ct_env = std::getenv("MOELORA_PF_CTAS");
+  const long long mb = mb_env ? std::atoll(mb_env) : 16;
+  const int ctas = ct_env ? std::atoi(ct_env) : 32;
+  if (!ok || !w || mb <= 0 || ctas <= 0 || expert_bytes < 16) return;
+  a.pf_base = static_cast<const unsigned char*>(w);
+  a.pf_expert_bytes = expert_bytes & ~15ll;
+  a.pf_bytes = mb << 20;
+  a.pf_ctas = std::min(ctas, 64);
+}
+
 cudaError_t run_align(Launcher& ln, AlignArgs a, cudaStream_t stream, int num_sms, bool* gathered) {
   cudaError_t e;
   if (gathered) *gathered = false;
@@ -980,6 +1001,7 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
     a.x_perm = reinterpret_cast<uint4*>(x_perm);
     a.hv = p.H / 8;
   }
+  set_prefetch(a, W_gate_up, 2ll * p.I * p.H * 2, !routed && p.gksplit == 1);
   bool gathered = false;
   MOELORA_CUDA_CHECK(run_align(ln, a, stream, sms, &gathered));
   if (!gathered) {
@@ -1115,6 +1137,7 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   a.x = reinterpret_cast<const uint4*>(x);
   a.x_perm = reinterpret_cast<uint4*>(x_perm);
   a.hv = p.H / 8;
+  set_prefetch(a, W, static_cast<long long>(p.N) * p.H * 2, p.ksplit == 1);
   bool gathered = false;
   MOELORA_CUDA_CHECK(run_align(ln, a, stream, sms, &gathered));
   if (!gathered) {
