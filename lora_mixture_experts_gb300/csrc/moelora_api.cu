@@ -62,9 +62,12 @@ struct Bump {
 };
 
 // Tuning overrides for benchmarking: MOELORA_KSPLIT (1..4), MOELORA_TN
-// (16, 32, 64, 128, 256) and MOELORA_GROUP_TILES (token tiles per group of
-// the GEMM item order).  Read at planning time, so the workspace size and
-// the call agree; unset means the built-in choice.
+// (16, 32, 64, 128, 256), MOELORA_GROUP_TILES (at most this many token tiles
+// per L2 group of the GEMM item order), MOELORA_GU_KSPLIT, MOELORA_TWO_PHASE,
+// MOELORA_SHRINK_SPLITS, MOELORA_SPREAD_SHRINK (0 / 1) and MOELORA_PF_MB /
+// MOELORA_PF_CTAS (the small align's weight prefetch).  Read at planning
+// time, so the workspace size and the call agree; unset means the built-in
+// choice.
 int env_override(const char* name, int lo, int hi) {
   const char* v = std::getenv(name);
   if (!v) return 0;
