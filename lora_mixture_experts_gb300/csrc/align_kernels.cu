@@ -383,6 +383,13 @@ __global__ void __launch_bounds__(kScanThreads) align_scan_kernel(AlignArgs a) {
   align_tables(a, warp_sums, sb);
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes 16-byte multiples).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Weight prefetch of the small align: CTA pi of n_pf counts the entries of
 // each expert, ranks the routed experts in expert order (the order of their
 // token tiles, and so of the first GEMM phase's main items), and issues its
