@@ -70,13 +70,23 @@ struct AlignArgs {
   const uint4* x;
   uint4* x_perm;
   int hv;
-  // L2 prefetch by extra CTAs of the small align (pf_ctas > 0): the weight
-  // rows that the first GEMM phase streams first, which are its routed
-  // experts' weights in expert order, pf_expert_bytes each (16-byte
-  // multiples from pf_base), up to pf_bytes, while the tables are built
+  // L2 prefetch by extra CTAs of the small align (pf_ctas > 0): the weights
+  // that the first GEMM phase streams first, up to pf_bytes, while the
+  // tables are built.  That phase's main items take the routed experts in
+  // expert order (pf_expert_bytes apart from pf_base) and each expert's
+  // weight tiles m = 0, 1, ...; weight tile m is rows [m * pf_rows_per_m,
+  // +pf_rows_per_m) of the pf_feat_rows feature rows, and the same rows
+  // pf_up_rows further on when that is not 0 (gate_up's up rows), and its
+  // first K split reads bytes [pf_seg0, pf_seg1) of each pf_row_bytes row.
   const unsigned char* pf_base;
   long long pf_expert_bytes;
   long long pf_bytes;
+  long long pf_row_bytes;
+  long long pf_seg0, pf_seg1;
+  long long pf_up_rows;
+  int pf_rows_per_m;
+  int pf_feat_rows;
+  int pf_n_m;
   int pf_ctas;
 };
 

@@ -390,13 +390,15 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
                : "memory");
 }
 
-// Weight prefetch of the small align: CTA pi of n_pf counts the entries of
-// each expert, ranks the routed experts in expert order (the order of their
-// token tiles, and so of the first GEMM phase's main items), and issues its
-// share of 64 KB L2 prefetches over the first routed experts' weights, up to
-// pf_bytes.  The copies run in the memory system while the align's other
-// CTAs build the tables, so the GEMM's first items read them from L2 instead
-// of HBM, which the align leaves idle.  Nothing is written; the CTA returns.
+// Weight prefetch of the small align: CTA pi of n_pf flags the experts that
+// have entries, ranks them in expert order (the order of their token tiles,
+// and so of the first GEMM phase's main items), and issues its share of L2
+// prefetches of what that phase reads first: whole experts in 64 KB pieces
+// when it does not split K, else the first split's slice of each weight
+// row, weight tile by weight tile, up to pf_bytes.  The copies run in the
+// memory system while the align's other CTAs build the tables, so the GEMM's
+// first items read them from L2 instead of HBM, which the align leaves
+// idle.  Nothing is written; the CTA returns.
 __device__ void align_prefetch(const AlignArgs& a, int* warp_sums, int* cnt, int pi, int n_pf) {
   __shared__ int s_list[8];   // routed experts, in order, whose bytes are prefetched
   const int tid = threadIdx.x;
@@ -411,20 +413,42 @@ __device__ void align_prefetch(const AlignArgs& a, int* warp_sums, int* cnt, int
   int n_routed;
   const int rank = block_exclusive_scan(routed ? 1 : 0, warp_sums, &n_routed);
   const long long eb = a.pf_expert_bytes;
-  const int n_list = static_cast<int>(min(static_cast<long long>(min(n_routed, 8)), (a.pf_bytes + eb - 1) / eb));
+  const long long seg = a.pf_seg1 - a.pf_seg0;
+  const bool whole = a.pf_seg0 == 0 && seg == a.pf_row_bytes;
+  const int rpt = a.pf_rows_per_m * (a.pf_up_rows ? 2 : 1);   // rows per weight tile
+  const long long per_expert = static_cast<long long>(a.pf_n_m) * rpt;
+  const long long want = whole ? (a.pf_bytes + eb - 1) / eb : (a.pf_bytes / seg + per_expert - 1) / per_expert;
+  const int n_list = static_cast<int>(min(static_cast<long long>(min(n_routed, 8)), want));
   if (routed && rank < n_list) s_list[rank] = tid;
   __syncthreads();
-  const long long total = min(a.pf_bytes, n_list * eb) & ~15ll;
-  constexpr long long kChunk = 1 << 16;
-  const long long n_chunks = (total + kChunk - 1) / kChunk;
-  for (long long c = pi + static_cast<long long>(n_pf) * tid; c < n_chunks;
-       c += static_cast<long long>(n_pf) * blockDim.x) {
-    const long long off = c * kChunk;
-    const int li = static_cast<int>(off / eb);
-    const long long o = off - li * eb;
-    const long long bytes = min(min(kChunk, eb - o), total - off);
-    if (bytes >= 16)
-      prefetch_l2_bulk(a.pf_base + static_cast<long long>(s_list[li]) * eb + o, static_cast<uint32_t>(bytes & ~15ll));
+  if (whole) {
+    const long long total = min(a.pf_bytes, n_list * eb) & ~15ll;
+    constexpr long long kChunk = 1 << 16;
+    const long long n_chunks = (total + kChunk - 1) / kChunk;
+    for (long long c = pi + static_cast<long long>(n_pf) * tid; c < n_chunks;
+         c += static_cast<long long>(n_pf) * blockDim.x) {
+      const long long off = c * kChunk;
+      const int li = static_cast<int>(off / eb);
+      const long long o = off - li * eb;
+      const long long bytes = min(min(kChunk, eb - o), total - off);
+      if (bytes >= 16)
+        prefetch_l2_bulk(a.pf_base + static_cast<long long>(s_list[li]) * eb + o,
+                         static_cast<uint32_t>(bytes & ~15ll));
+    }
+    return;
+  }
+  const long long units = min(a.pf_bytes / seg, n_list * per_expert);
+  for (long long u = pi + static_cast<long long>(n_pf) * tid; u < units;
+       u += static_cast<long long>(n_pf) * blockDim.x) {
+    const int li = static_cast<int>(u / per_expert);
+    const long long rem = u - li * per_expert;
+    const int m = static_cast<int>(rem / rpt);
+    const int q = static_cast<int>(rem - static_cast<long long>(m) * rpt);
+    const int fr = m * a.pf_rows_per_m + (q < a.pf_rows_per_m ? q : q - a.pf_rows_per_m);
+    if (fr >= a.pf_feat_rows) continue;
+    const long long row = fr + (q < a.pf_rows_per_m ? 0 : a.pf_up_rows);
+    prefetch_l2_bulk(a.pf_base + static_cast<long long>(s_list[li]) * eb + row * a.pf_row_bytes + a.pf_seg0,
+                     static_cast<uint32_t>(seg));
   }
 }
 

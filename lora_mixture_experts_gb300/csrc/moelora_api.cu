@@ -616,23 +616,36 @@ struct Launcher {
 constexpr size_t kFusedGatherBytes = 512 * 1024;
 
 // L2 prefetch by extra CTAs of the small align (see align_prefetch) of the
-// weights that the first GEMM phase streams first: its routed experts' whole
-// weights in expert order, which is what that phase reads first when it
-// does not split K.  Budget and CTAs measured on the GB300 (decode 237.0 ->
-// 236.1 us, dense MLP T = 64 189.2 -> 188.3 us with 16 MB over 32 CTAs; 40
-// and 80 MB were slower than none: the prefetch then competes with the
-// GEMM's own first loads).  MOELORA_PF_MB / MOELORA_PF_CTAS override them
-// (0 turns the prefetch off).
-void set_prefetch(AlignArgs& a, const void* w, long long expert_bytes, bool ok) {
+// weights that the first GEMM phase streams first: its first routed
+// experts' weight tiles in item order, the whole rows when the phase does
+// not split K, else the first split's slice of each row.  Budget and CTAs
+// measured on the GB300 (decode 237.0 -> 236.1 us, dense MLP T = 64 189.2
+// -> 188.3 us with 16 MB over 32 CTAs; 40 and 80 MB were slower than none:
+// the prefetch then competes with the GEMM's own first loads).
+// MOELORA_PF_MB / MOELORA_PF_CTAS override them (0 turns the prefetch off).
+// The first phase: weight w, expert_bytes apart; rows of K bf16; weight tile
+// m = feature rows [m * rows_per_m, +rows_per_m) and, for gate_up, the same
+// rows up_rows further on; its first K split ends at K block k1 of bk.
+void set_prefetch(AlignArgs& a, const void* w, long long expert_bytes, int K, int feat_rows,
+                  int rows_per_m, long long up_rows, int n_m, int k1_blocks, int bk, bool ok) {
   a.pf_ctas = 0;
   const char* mb_env = std::getenv("MOELORA_PF_MB");
   const char* ct_env = std::getenv("MOELORA_PF_CTAS");
   const long long mb = mb_env ? std::atoll(mb_env) : 16;
   const int ctas = ct_env ? std::atoi(ct_env) : 32;
-  if (!ok || !w || mb <= 0 || ctas <= 0 || expert_bytes < 16) return;
+  const long long row_bytes = 2ll * K;
+  const long long seg1 = std::min<long long>(K, static_cast<long long>(k1_blocks) * bk) * 2;
+  if (!ok || !w || mb <= 0 || ctas <= 0 || expert_bytes < 16 || seg1 < 16 || (seg1 & 15)) return;
   a.pf_base = static_cast<const unsigned char*>(w);
   a.pf_expert_bytes = expert_bytes & ~15ll;
   a.pf_bytes = mb << 20;
+  a.pf_row_bytes = row_bytes;
+  a.pf_seg0 = 0;
+  a.pf_seg1 = seg1;
+  a.pf_up_rows = up_rows;
+  a.pf_rows_per_m = rows_per_m;
+  a.pf_feat_rows = feat_rows;
+  a.pf_n_m = n_m;
   a.pf_ctas = std::min(ctas, 64);
 }
 
@@ -1004,7 +1017,8 @@ int forward_impl(const moelora_dims* d, const moelora_bf16* x, const int32_t* to
     a.x_perm = reinterpret_cast<uint4*>(x_perm);
     a.hv = p.H / 8;
   }
-  set_prefetch(a, W_gate_up, 2ll * p.I * p.H * 2, !routed && p.gksplit == 1);
+  set_prefetch(a, W_gate_up, 2ll * p.I * p.H * 2, p.H, p.I, paired ? 128 : 64, p.I, gu.n_mtiles,
+               gu.split_k0[1], static_cast<int>(bk), !routed);
   bool gathered = false;
   MOELORA_CUDA_CHECK(run_align(ln, a, stream, sms, &gathered));
   if (!gathered) {
@@ -1140,7 +1154,8 @@ int moe_lora_linear(const moelora_linear_dims* d, const moelora_bf16* x, const i
   a.x = reinterpret_cast<const uint4*>(x);
   a.x_perm = reinterpret_cast<uint4*>(x_perm);
   a.hv = p.H / 8;
-  set_prefetch(a, W, static_cast<long long>(p.N) * p.H * 2, p.ksplit == 1);
+  set_prefetch(a, W, static_cast<long long>(p.N) * p.H * 2, p.H, p.N, paired ? 256 : 128, 0, g.n_mtiles,
+               g.split_k0[1], static_cast<int>(bk), true);
   bool gathered = false;
   MOELORA_CUDA_CHECK(run_align(ln, a, stream, sms, &gathered));
   if (!gathered) {
