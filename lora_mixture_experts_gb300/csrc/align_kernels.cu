@@ -463,6 +463,18 @@ __device__ void align_prefetch(const AlignArgs& a, int* warp_sums, int* cnt, int
 __global__ void __launch_bounds__(kScanThreads, 1) align_small_kernel(AlignArgs a) {
   __shared__ int warp_sums[96];
   extern __shared__ int sm_bins[];   // [nbins] running counts, then [n] positions (gather)
+  // The last pf_ctas CTAs prefetch weights into L2 (no router here: the ids
+  // are inputs).  A prefetch writes nothing and L2 is coherent, so they do
+  // not wait for the preceding kernel: ids read before it has finished can
+  // at worst aim the prefetch at the wrong weights (ids out of range are
+  // skipped), and starting during the preceding kernel gives the copies more
+  // of the time the HBM would sit idle.
+  const int n_pf = a.pf_ctas > 0 && a.pf_base && !a.logits ? a.pf_ctas : 0;
+  if (static_cast<int>(blockIdx.x) >= static_cast<int>(gridDim.x) - n_pf) {
+    align_prefetch(a, warp_sums, sm_bins, static_cast<int>(blockIdx.x) - (static_cast<int>(gridDim.x) - n_pf),
+                   n_pf);
+    return;
+  }
   grid_dependency_wait();
   grid_dependency_trigger();
   const int tid = threadIdx.x;
@@ -473,13 +485,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) align_small_kernel(AlignArgs 
   if (a.reset_err && tables) {   // the call's first kernel clears the error word itself
     if (tid == 0) a.hdr->err = 0;
     __syncthreads();
-  }
-  // the last pf_ctas CTAs prefetch weights (no router here: the ids are inputs)
-  const int n_pf = a.pf_ctas > 0 && a.pf_base && !a.logits ? a.pf_ctas : 0;
-  if (static_cast<int>(blockIdx.x) >= static_cast<int>(gridDim.x) - n_pf) {
-    align_prefetch(a, warp_sums, sm_bins, static_cast<int>(blockIdx.x) - (static_cast<int>(gridDim.x) - n_pf),
-                   n_pf);
-    return;
   }
   const int gx = static_cast<int>(gridDim.x) - n_pf;   // the table and copying CTAs
   const int lane = tid & 31;

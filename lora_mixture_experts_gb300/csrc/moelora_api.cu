@@ -618,10 +618,12 @@ constexpr size_t kFusedGatherBytes = 512 * 1024;
 // L2 prefetch by extra CTAs of the small align (see align_prefetch) of the
 // weights that the first GEMM phase streams first: its first routed
 // experts' weight tiles in item order, the whole rows when the phase does
-// not split K, else the first split's slice of each row.  Budget and CTAs
-// measured on the GB300 (decode 237.0 -> 236.1 us, dense MLP T = 64 189.2
-// -> 188.3 us with 16 MB over 32 CTAs; 40 and 80 MB were slower than none:
-// the prefetch then competes with the GEMM's own first loads).
+// not split K, else the first split's slice of each row.  Budgets measured
+// on the GB300 with the prefetching CTAs starting before the preceding
+// kernel ends (32 CTAs): whole experts 24 MB (decode 237.0 -> 234.8 us
+// against none; 16 MB 235.3, 32 MB 237.3, 48 MB 236.1: more competes with the
+// GEMM's own first loads), row slices 32 MB (dense T = 1 85.4 -> 83.0 us, T =
+// 8 -> 87.7 us, dense MLP T = 1 -> 125.8 us; 64 MB slower).
 // MOELORA_PF_MB / MOELORA_PF_CTAS override them (0 turns the prefetch off).
 // The first phase: weight w, expert_bytes apart; rows of K bf16; weight tile
 // m = feature rows [m * rows_per_m, +rows_per_m) and, for gate_up, the same
@@ -633,8 +635,7 @@ void set_prefetch(AlignArgs& a, const void* w, long long expert_bytes, int K, in
   const char* ct_env = std::getenv("MOELORA_PF_CTAS");
   const long long row_bytes = 2ll * K;
   const long long seg1 = std::min<long long>(K, static_cast<long long>(k1_blocks) * bk) * 2;
-  // (row slices: 24 MB measured best, dense T = 1 84.0 -> 83.4 us against 16 MB)
-  const long long mb = mb_env ? std::atoll(mb_env) : (seg1 < row_bytes ? 24 : 16);
+  const long long mb = mb_env ? std::atoll(mb_env) : (seg1 < row_bytes ? 32 : 24);
   const int ctas = ct_env ? std::atoi(ct_env) : 32;
   if (!ok || !w || mb <= 0 || ctas <= 0 || expert_bytes < 16 || seg1 < 16 || (seg1 & 15)) return;
   a.pf_base = static_cast<const unsigned char*>(w);
