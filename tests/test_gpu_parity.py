@@ -331,6 +331,34 @@ def test_linear_spread_shrink_order(monkeypatch, spread):
     assert torch.equal(out, binding.moe_lora_linear(x, lo, W, A, B))
 
 
+@pytest.mark.parametrize("name", ["decode", "dense_mlp_t1", "tiny"])
+def test_align_weight_prefetch_changes_no_bit(monkeypatch, name):
+    """The small align's L2 weight prefetch (whole experts for the decode
+    batch, the first K split's row slices for the dense MLP at T = 1) only
+    moves lines into L2: the output is the same bits with it off, and the
+    batch still matches the oracle."""
+    c = CONFIGS[name]
+    d = make_moe_case(c, seed=0, device=DEV)
+    out = _gpu_forward(d).clone()
+    monkeypatch.setenv("MOELORA_PF_MB", "0")
+    assert torch.equal(out, _gpu_forward(d))
+    monkeypatch.setenv("MOELORA_PF_MB", "64")      # a larger prefetch, still no effect on the bits
+    assert torch.equal(out, _gpu_forward(d))
+    if name == "tiny":
+        n = np_inputs(d)
+        ok, msg = compare(out, _oracle_forward(n), f"{name} with the prefetch")
+        assert ok, msg
+
+
+def test_linear_weight_prefetch_changes_no_bit(monkeypatch):
+    """The dense linear's align prefetch (row slices of the first K split):
+    the same bits with it off."""
+    d = make_linear_case(CONFIGS["dense_t1"], seed=0, device=DEV)
+    out = binding.moe_lora_linear(d["x"], d["lora_ids"], d["W"], d["A"], d["B"]).clone()
+    monkeypatch.setenv("MOELORA_PF_MB", "0")
+    assert torch.equal(out, binding.moe_lora_linear(d["x"], d["lora_ids"], d["W"], d["A"], d["B"]))
+
+
 @pytest.mark.parametrize("shape", _random_shapes(24, 17), ids=lambda s: "T{T}_H{H}_I{I}_E{E}_k{k}_L{L}_r{r}".format(**s))
 def test_forward_random_shapes(shape):
     s = shape
