@@ -37,12 +37,14 @@
 // blocks (64 KB), which is what the tensor-bound prefill tiles need: TMA
 // streaming from L2 measured 9 TB/s with 16 KB stages but 19-25 TB/s with 64 KB.
 //
-// Shrink items precede main items in the item order and a main item's
-// producer waits (bounded) for its tile's shrink items before loading the
-// z chunks.  Items are claimed in index order from a counter by CTAs (CTA
-// pairs) that are running, so every item waited for was claimed earlier by a
-// running CTA and the wait ends even when only part of the grid is resident
-// (another stream's kernels holding SMs).
+// A tile's shrink items precede its main items in the item order (all
+// shrink items first, or, in large CTA-pair launches, each tile's a wave of
+// items ahead of it: see ItemOrder), and a main item's producer waits
+// (bounded) for its tile's shrink items before loading the z chunks.  Items
+// are claimed in index order from a counter by CTAs (CTA pairs) that are
+// running, so every item waited for was claimed earlier by a running CTA and
+// the wait ends even when only part of the grid is resident (another
+// stream's kernels holding SMs).
 #include "gemm_tc.cuh"
 
 #include <algorithm>
